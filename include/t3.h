@@ -1,0 +1,123 @@
+/*
+ * t3.h -- C ABI of the ternary-weight x int8 GEMM library for GB300 (sm_103a).
+ *
+ * Three integer products of a ternary-weight layer and the packer of its
+ * weights.  All results are exact int32; there is no rounding, no scale and no
+ * tolerance on this path.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [fwd] "t27c PTX backend: ternary x int8 GEMM kernel emitted by a .t27 spec
+ *         (int8 mma.sync), ptx-run glue", section "What this adds": C = A x W
+ *         with int8 A and ternary W held as 2-bit codes, each decoded as
+ *         (c & 1) - ((c >> 1) & 1), i.e. 0 -> 0, 1 -> +1, 2 -> -1, 3 -> 0.
+ *   [bwd] "spec(igla): hslm_bwd_ptx -- HSLM backward dX and dW as int8
+ *         tensor-core PTX written by t27", kernel 1 (dX = dY x W^T, W ternary
+ *         in the same code layout) and kernel 2 (dW = X^T x dY summed over
+ *         rows, int32 accumulation, reduction length <= 131071).
+ *
+ * Layouts (all row-major and densely packed, no row padding):
+ *   A  int8  [M][K]          activations
+ *   Wp uint8 [N][ceil(K/4)]  packed weights: the code of W[k][n] is at bits
+ *                            2*(k%4) of byte k/4 of row n; positions k >= K of
+ *                            the last byte of a row are ignored by every call.
+ *   C  int32 [M][N]          forward output
+ *   dY int8  [M][N]          output gradient
+ *   dX int32 [M][K]          input gradient
+ *   dW int32 [K][N]          weight gradient
+ *
+ * Ownership and threading:
+ *   - The caller owns every buffer.  The GEMM calls take DEVICE pointers (any
+ *     memory the current device can read/write), enqueue their work on
+ *     `stream` and return without waiting; the results are ready once the
+ *     stream reaches that point.  The library allocates no device memory per
+ *     call.
+ *   - Outputs are overwritten, never accumulated into.
+ *   - A call with M, N or K equal to 0 does nothing and returns T3_OK.
+ *   - Argument errors are reported before anything is launched; nothing is
+ *     written then.  No C++ exception crosses this interface and the device
+ *     code never traps.
+ *   - Calls may be made from several host threads; each call is independent.
+ */
+#ifndef T3_H_
+#define T3_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (the same type as cudaStream_t / CUstream); NULL is the
+ * legacy default stream. */
+typedef struct CUstream_st* t3_stream_t;
+
+typedef enum {
+  T3_OK = 0,
+  T3_EINVAL = -1,     /* null pointer with a non-empty shape, negative size   */
+  T3_EVALUE = -2,     /* t3_pack_ternary: a weight outside {-1, 0, +1}        */
+  T3_EOVERFLOW = -3,  /* a reduction too long for an exact int32 result       */
+  T3_ECUDA = -4,      /* a CUDA runtime/driver call failed (launch, attribute) */
+  T3_ETIMEOUT = -5,   /* a bounded device-side wait gave up (see below)       */
+  T3_EDEVICE = -6     /* no usable sm_103 device for this call               */
+} t3_status;
+
+/*
+ * t3_pack_ternary -- [fwd] "What this adds" (the 2-bit weight codes).
+ *   w   HOST int8 [K][N], every value in {-1, 0, +1} (W as it appears in A x W)
+ *   wp  HOST uint8 [N][ceil(K/4)], written in full: code 1 for +1, 2 for -1,
+ *       0 for 0 and for the pad positions k >= K.
+ * Synchronous, host memory only.  Returns T3_EVALUE and writes nothing when a
+ * value is outside {-1, 0, +1}; T3_EINVAL for negative sizes or null pointers.
+ */
+int t3_pack_ternary(const int8_t* w, uint8_t* wp, int64_t K, int64_t N);
+
+/*
+ * t3_gemm_fwd -- [fwd]: C[m][n] = sum_{k<K} A[m][k] * W[k][n].
+ *   A [M][K], Wp [N][ceil(K/4)], C [M][N] (layouts above), device pointers.
+ * Exact for every input when K <= 16777215 (|A W| <= 128 K fits int32);
+ * larger K returns T3_EOVERFLOW.  M <= 32 takes the small-M path, which is
+ * bound by reading the packed weights.
+ */
+int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,
+                int64_t K, t3_stream_t stream);
+
+/*
+ * t3_gemm_bwd_dx -- [bwd] kernel 1: dX[m][k] = sum_{n<N} dY[m][n] * W[k][n].
+ *   dY [M][N], Wp [N][ceil(K/4)] (the forward's packed weights), dX [M][K].
+ * Exact for every input when N <= 16777215; larger N returns T3_EOVERFLOW.
+ */
+int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, int64_t N,
+                   int64_t K, t3_stream_t stream);
+
+/*
+ * t3_gemm_bwd_dw -- [bwd] kernel 2: dW[k][n] = sum_{m<M} A[m][k] * dY[m][n].
+ *   A [M][K], dY [M][N], dW [K][N].
+ * int8 x int8 products reach 16384, so the reduction is exact in int32 only
+ * for M <= 131071 (the pages' bound); larger M returns T3_EOVERFLOW.
+ */
+int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N,
+                   int64_t K, t3_stream_t stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+const char* t3_status_string(int status);
+
+/*
+ * t3_last_device_error -- every pipeline wait inside the kernels is bounded
+ * (about two seconds of device time).  A wait that runs out makes its kernel
+ * stop early, leaving its output incomplete, and records a code in a
+ * per-device error word instead of hanging the GPU.  This call synchronizes
+ * `stream`, returns T3_ETIMEOUT if the word is set (T3_OK otherwise) and
+ * clears it.  *detail, when not NULL, receives the recorded code (0 if none):
+ * bits 0-7 the role that gave up (1 producer, 2 converter, 3 MMA issuer,
+ * 4 epilogue), bits 8-15 the kernel (1 fwd, 2 dX, 3 dW, 4 small-M fwd).
+ */
+int t3_last_device_error(t3_stream_t stream, int32_t* detail);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int t3_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* T3_H_ */

@@ -1,0 +1,202 @@
+"""Python binding of the t3 C ABI (include/t3.h): argument marshalling only.
+
+Every product runs in the CUDA kernels of ``libt3.so``; this module checks
+dtypes, shapes and devices, allocates outputs with torch when the caller does
+not pass them, and forwards raw pointers and the current CUDA stream.  There
+is no fallback: if the library is missing or cannot load, every call raises.
+
+Function names follow the C ABI:
+  t3_pack_ternary(w)                       host packer, w int8 [K][N]
+  t3_gemm_fwd(A, Wp, K=None, C=None)       C  = A . W        (int32 [M][N])
+  t3_gemm_bwd_dx(dY, Wp, K, dX=None)       dX = dY . W^T     (int32 [M][K])
+  t3_gemm_bwd_dw(A, dY, dW=None)           dW = A^T . dY     (int32 [K][N])
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libt3.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "t3.h")
+
+T3_OK, T3_EINVAL, T3_EVALUE, T3_EOVERFLOW, T3_ECUDA, T3_ETIMEOUT, T3_EDEVICE = 0, -1, -2, -3, -4, -5, -6
+
+_lock = threading.Lock()
+_lib = None
+
+
+class T3Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def build(force: bool = False) -> str:
+    """Compiles libt3.so for sm_103a (nvcc); returns its path."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def load():
+    """Loads libt3.so (building it first if it is absent or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        from . import _build
+        if not _build.up_to_date():
+            _build.build()
+        lib = ctypes.CDLL(LIB_PATH)
+        p, i64 = ctypes.c_void_p, ctypes.c_int64
+        lib.t3_pack_ternary.argtypes = [p, p, i64, i64]
+        for name in ("t3_gemm_fwd", "t3_gemm_bwd_dx", "t3_gemm_bwd_dw"):
+            f = getattr(lib, name)
+            f.argtypes = [p, p, p, i64, i64, i64, p]
+            f.restype = ctypes.c_int
+        lib.t3_pack_ternary.restype = ctypes.c_int
+        lib.t3_status_string.argtypes = [ctypes.c_int]
+        lib.t3_status_string.restype = ctypes.c_char_p
+        lib.t3_last_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
+        lib.t3_last_device_error.restype = ctypes.c_int
+        lib.t3_version.argtypes = []
+        lib.t3_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/t3.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(t3_\w+)\s*\(", text, re.M)))
+
+
+def status_string(status: int) -> str:
+    return load().t3_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != T3_OK:
+        raise T3Error(status, where)
+
+
+# ------------------------------------------------------------------- host ---
+
+def t3_pack_ternary(w) -> np.ndarray:
+    """Packs ternary w (int8 [K][N], values in {-1,0,+1}; numpy or CPU tensor)
+    into Wp (uint8 [N][ceil(K/4)]) with the library's host packer."""
+    if hasattr(w, "detach"):
+        w = w.detach().cpu().numpy()
+    w = np.ascontiguousarray(w)
+    if w.dtype != np.int8 or w.ndim != 2:
+        raise TypeError("w must be a 2-D int8 array [K][N]")
+    K, N = w.shape
+    wp = np.empty((N, (K + 3) // 4), dtype=np.uint8)
+    rc = load().t3_pack_ternary(ctypes.c_void_p(w.ctypes.data), ctypes.c_void_p(wp.ctypes.data),
+                                K, N)
+    _check(rc, "t3_pack_ternary")
+    return wp
+
+
+# ----------------------------------------------------------------- device ---
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev_ptr(t, dtype, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr() if t.numel() else 0)
+
+
+def _stream(t, stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def t3_gemm_fwd(A, Wp, K: int | None = None, C=None, stream=None):
+    """C[m][n] = sum_k A[m][k] W[k][n].  A int8 [M][K], Wp uint8 [N][ceil(K/4)]."""
+    torch = _torch()
+    M, Ka = A.shape
+    K = Ka if K is None else K
+    if Ka != K:
+        raise ValueError("A must be [M][K]")
+    N = Wp.shape[0]
+    if Wp.dim() != 2 or Wp.shape[1] != (K + 3) // 4:
+        raise ValueError("Wp must be [N][ceil(K/4)]")
+    if C is None:
+        _dev_ptr(A, torch.int8, "A")
+        C = torch.empty((M, N), dtype=torch.int32, device=A.device)
+    elif tuple(C.shape) != (M, N):
+        raise ValueError("C must be [M][N]")
+    args = (_dev_ptr(A, torch.int8, "A"), _dev_ptr(Wp, torch.uint8, "Wp"),
+            _dev_ptr(C, torch.int32, "C"))
+    with torch.cuda.device(A.device):
+        rc = load().t3_gemm_fwd(*args, M, N, K, _stream(A, stream))
+    _check(rc, "t3_gemm_fwd")
+    return C
+
+
+def t3_gemm_bwd_dx(dY, Wp, K: int, dX=None, stream=None):
+    """dX[m][k] = sum_n dY[m][n] W[k][n].  dY int8 [M][N], Wp uint8 [N][ceil(K/4)]."""
+    torch = _torch()
+    M, N = dY.shape
+    if Wp.dim() != 2 or tuple(Wp.shape) != (N, (K + 3) // 4):
+        raise ValueError("Wp must be [N][ceil(K/4)]")
+    if dX is None:
+        _dev_ptr(dY, torch.int8, "dY")
+        dX = torch.empty((M, K), dtype=torch.int32, device=dY.device)
+    elif tuple(dX.shape) != (M, K):
+        raise ValueError("dX must be [M][K]")
+    args = (_dev_ptr(dY, torch.int8, "dY"), _dev_ptr(Wp, torch.uint8, "Wp"),
+            _dev_ptr(dX, torch.int32, "dX"))
+    with torch.cuda.device(dY.device):
+        rc = load().t3_gemm_bwd_dx(*args, M, N, K, _stream(dY, stream))
+    _check(rc, "t3_gemm_bwd_dx")
+    return dX
+
+
+def t3_gemm_bwd_dw(A, dY, dW=None, stream=None):
+    """dW[k][n] = sum_m A[m][k] dY[m][n].  A int8 [M][K], dY int8 [M][N]."""
+    torch = _torch()
+    M, K = A.shape
+    if dY.shape[0] != M:
+        raise ValueError("A and dY must have the same number of rows")
+    N = dY.shape[1]
+    if dW is None:
+        _dev_ptr(A, torch.int8, "A")
+        dW = torch.empty((K, N), dtype=torch.int32, device=A.device)
+    elif tuple(dW.shape) != (K, N):
+        raise ValueError("dW must be [K][N]")
+    args = (_dev_ptr(A, torch.int8, "A"), _dev_ptr(dY, torch.int8, "dY"),
+            _dev_ptr(dW, torch.int32, "dW"))
+    with torch.cuda.device(A.device):
+        rc = load().t3_gemm_bwd_dw(*args, M, N, K, _stream(A, stream))
+    _check(rc, "t3_gemm_bwd_dw")
+    return dW
+
+
+def t3_last_device_error(stream=None):
+    """(status, detail): T3_ETIMEOUT and the recorded code if a bounded device
+    wait gave up since the last call; synchronizes the stream."""
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    detail = ctypes.c_int32(0)
+    rc = load().t3_last_device_error(ctypes.c_void_p(s.cuda_stream), ctypes.byref(detail))
+    return rc, detail.value
+
+
+def t3_version() -> int:
+    return load().t3_version()

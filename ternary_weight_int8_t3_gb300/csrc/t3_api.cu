@@ -1,0 +1,247 @@
+// t3_api.cu -- the C ABI: argument checks, the host packer, TMA descriptors,
+// launches and the device error word.  See include/t3.h for the contract.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/t3.h"
+#include "t3_internal.h"
+
+namespace t3 {
+
+// One error word per device (a __device__ variable has one instance per
+// device context).  Kernels receive its address; t3_last_device_error reads
+// and clears it.
+__device__ int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = 2147483647LL;           // TMA coordinates are int32
+constexpr int64_t kMaxTernaryReduction = 16777215;  // 128 * K <= INT32_MAX
+constexpr int64_t kMaxInt8Reduction = 131071;       // 16384 * M <= INT32_MAX
+
+struct DeviceInfo {
+  bool ready = false;
+  int status = T3_OK;
+  int sms = 0;
+  int* err_word = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+int device_info(const DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return T3_EDEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return T3_ECUDA;
+    if (major != 10 || minor != 3) {
+      d.status = T3_EDEVICE;  // built for sm_103a only
+    } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err_word), g_error_word) !=
+               cudaSuccess) {
+      return T3_ECUDA;
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return d.status;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Describes a row-major byte matrix [rows][cols] (row stride ld) for 2-D TMA
+// boxes of box_rows x box_cols.  Returns false when TMA cannot be used (base
+// or stride not 16-byte aligned, or the driver refuses); the kernel then
+// loads that operand with plain loads.
+bool make_u8_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                 int box_rows, int box_cols) {
+  std::memset(map, 0, sizeof(*map));
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || ld % 16 != 0) return false;
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+template <int OP>
+int run_tc(const uint8_t* a_src, int64_t a_rows, int64_t a_cols, const uint8_t* b_src,
+           int64_t b_rows, int64_t b_cols, int32_t* out, int64_t out_rows, int64_t out_cols,
+           int64_t reduction, int64_t chunk_kb, cudaStream_t stream) {
+  const DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != T3_OK) return st;
+  using R = tc::Raw<OP>;
+  tc::Params p{};
+  p.a_src = a_src;
+  p.a_ld = a_cols;
+  p.a_rows = a_rows;
+  p.a_cols = a_cols;
+  p.b_src = b_src;
+  p.b_ld = b_cols;
+  p.b_rows = b_rows;
+  p.b_cols = b_cols;
+  p.out = out;
+  p.out_rows = out_rows;
+  p.out_cols = out_cols;
+  p.num_kb = ceil_div(reduction, tc::BK);
+  p.chunk_kb = chunk_kb;
+  const int64_t tiles_r = ceil_div(out_rows, tc::BM), tiles_c = ceil_div(out_cols, tc::BN);
+  if (tiles_r * tiles_c > kMaxDim) return T3_EINVAL;
+  p.tiles_r = static_cast<int>(tiles_r);
+  p.tiles_c = static_cast<int>(tiles_c);
+  p.err = dev->err_word;
+  p.op_code = OP;
+  CUtensorMap ma, mb;
+  p.use_tma_a = make_u8_map(&ma, a_src, a_rows, a_cols, a_cols, R::a_rows, R::a_cols) ? 1 : 0;
+  p.use_tma_b = make_u8_map(&mb, b_src, b_rows, b_cols, b_cols, R::b_rows, R::b_cols) ? 1 : 0;
+  const int64_t tiles = tiles_r * tiles_c;
+  const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
+  if (OP == kOpFwd) return launch_tc_fwd(p, ma, mb, grid, stream);
+  if (OP == kOpDx) return launch_tc_dx(p, ma, mb, grid, stream);
+  return launch_tc_dw(p, ma, mb, grid, stream);
+}
+
+bool bad_dims(int64_t M, int64_t N, int64_t K) {
+  return M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim;
+}
+
+// Empty reduction: the output is all zeros.
+int zero_fill(int32_t* out, int64_t rows, int64_t cols, cudaStream_t s) {
+  if (!out) return T3_EINVAL;
+  return cudaMemsetAsync(out, 0, static_cast<size_t>(rows) * cols * sizeof(int32_t), s) ==
+                 cudaSuccess
+             ? T3_OK
+             : T3_ECUDA;
+}
+
+}  // namespace
+}  // namespace t3
+
+using namespace t3;
+
+extern "C" {
+
+int t3_pack_ternary(const int8_t* w, uint8_t* wp, int64_t K, int64_t N) {
+  if (K < 0 || N < 0) return T3_EINVAL;
+  if (K == 0 || N == 0) return T3_OK;
+  if (!w || !wp) return T3_EINVAL;
+  const int64_t total = K * N;
+  for (int64_t i = 0; i < total; ++i)
+    if (w[i] < -1 || w[i] > 1) return T3_EVALUE;
+  const int64_t KB = (K + 3) / 4;
+  for (int64_t kb = 0; kb < KB; ++kb) {
+    const int64_t k0 = 4 * kb;
+    const int nk = static_cast<int>(K - k0 < 4 ? K - k0 : 4);
+    for (int64_t n = 0; n < N; ++n) {
+      uint32_t byte = 0;
+      for (int j = 0; j < nk; ++j) {
+        const int8_t v = w[(k0 + j) * N + n];
+        const uint32_t code = v == 1 ? 1u : (v == -1 ? 2u : 0u);
+        byte |= code << (2 * j);
+      }
+      wp[n * KB + kb] = static_cast<uint8_t>(byte);
+    }
+  }
+  return T3_OK;
+}
+
+int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N, int64_t K,
+                t3_stream_t stream) {
+  if (bad_dims(M, N, K)) return T3_EINVAL;
+  if (M == 0 || N == 0) return T3_OK;
+  if (K == 0) return zero_fill(C, M, N, stream);
+  if (!A || !Wp || !C) return T3_EINVAL;
+  if (K > kMaxTernaryReduction) return T3_EOVERFLOW;
+  const int64_t KB = (K + 3) / 4;
+  return run_tc<kOpFwd>(reinterpret_cast<const uint8_t*>(A), M, K, Wp, N, KB, C, M, N, K,
+                        tc::kChunkKbTernary, stream);
+}
+
+int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, int64_t N,
+                   int64_t K, t3_stream_t stream) {
+  if (bad_dims(M, N, K)) return T3_EINVAL;
+  if (M == 0 || K == 0) return T3_OK;
+  if (N == 0) return zero_fill(dX, M, K, stream);
+  if (!dY || !Wp || !dX) return T3_EINVAL;
+  if (N > kMaxTernaryReduction) return T3_EOVERFLOW;
+  const int64_t KB = (K + 3) / 4;
+  return run_tc<kOpDx>(reinterpret_cast<const uint8_t*>(dY), M, N, Wp, N, KB, dX, M, K, N,
+                       tc::kChunkKbTernary, stream);
+}
+
+int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N,
+                   int64_t K, t3_stream_t stream) {
+  if (bad_dims(M, N, K)) return T3_EINVAL;
+  if (K == 0 || N == 0) return T3_OK;
+  if (M == 0) return zero_fill(dW, K, N, stream);
+  if (!A || !dY || !dW) return T3_EINVAL;
+  if (M > kMaxInt8Reduction) return T3_EOVERFLOW;
+  return run_tc<kOpDw>(reinterpret_cast<const uint8_t*>(A), M, K,
+                       reinterpret_cast<const uint8_t*>(dY), M, N, dW, K, N, M,
+                       tc::kChunkKbInt8, stream);
+}
+
+const char* t3_status_string(int status) {
+  switch (status) {
+    case T3_OK: return "T3_OK: success";
+    case T3_EINVAL: return "T3_EINVAL: null pointer or invalid size";
+    case T3_EVALUE: return "T3_EVALUE: weight outside {-1, 0, +1}";
+    case T3_EOVERFLOW: return "T3_EOVERFLOW: reduction too long for an exact int32 result";
+    case T3_ECUDA: return "T3_ECUDA: a CUDA call failed";
+    case T3_ETIMEOUT: return "T3_ETIMEOUT: a bounded device wait gave up";
+    case T3_EDEVICE: return "T3_EDEVICE: no usable sm_103 device";
+    default: return "unknown t3 status";
+  }
+}
+
+int t3_last_device_error(t3_stream_t stream, int32_t* detail) {
+  if (detail) *detail = 0;
+  const DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != T3_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return T3_ECUDA;
+  int value = 0;
+  if (cudaMemcpy(&value, dev->err_word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return T3_ECUDA;
+  if (value != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(dev->err_word, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return T3_ECUDA;
+  }
+  if (detail) *detail = value;
+  return value ? T3_ETIMEOUT : T3_OK;
+}
+
+int t3_version(void) { return 100; }
+
+}  // extern "C"

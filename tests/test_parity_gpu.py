@@ -1,0 +1,265 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, bit-exact.
+
+Inputs come from t3_synth (seeded); the weights are packed by the library's
+packer for the GPU and by the oracle's own packer for the oracle (the two are
+compared in the CPU tests).  Small and ragged shapes are compared element by
+element in full; the full-size workloads, in the launch configuration the
+bench uses, are compared on sampled rows that the oracle computes one by one.
+Output buffers carry canary words before and after the result.
+"""
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import t3_synth
+import ternary_weight_int8_t3_gb300 as t3
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+CANARY = 0x5A5A5A5A - (1 << 32)  # an int32 no product here can produce by accident
+PAD = 64                         # canary words on each side of an output
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    major, minor = torch.cuda.get_device_capability(0)
+    assert (major, minor) == (10, 3), f"built for sm_103a, found sm_{major}{minor}"
+    t3.load()
+    yield
+    torch.cuda.synchronize()
+    rc, detail = t3.t3_last_device_error()
+    assert rc == t3.T3_OK, f"device wait timed out, detail={detail:#x}"
+
+
+@functools.lru_cache(maxsize=4)
+def workload_inputs(name):
+    return t3_synth.make_inputs(t3_synth.BY_NAME[name])
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _guarded(rows, cols):
+    buf = torch.full((rows * cols + 2 * PAD,), CANARY, dtype=torch.int32, device="cuda")
+    return buf, buf[PAD:PAD + rows * cols].view(rows, cols)
+
+
+def _check_guard(buf, rows, cols):
+    h = buf.cpu().numpy()
+    assert np.all(h[:PAD] == CANARY) and np.all(h[PAD + rows * cols:] == CANARY), "canary overwritten"
+
+
+def run_fwd(A, wp):
+    M, K = A.shape
+    N = wp.shape[0]
+    buf, C = _guarded(M, N)
+    t3.t3_gemm_fwd(_dev(A), _dev(wp), K=K, C=C)
+    torch.cuda.synchronize()
+    _check_guard(buf, M, N)
+    return C.cpu().numpy()
+
+
+def run_dx(dY, wp, K):
+    M, N = dY.shape
+    buf, dX = _guarded(M, K)
+    t3.t3_gemm_bwd_dx(_dev(dY), _dev(wp), K, dX=dX)
+    torch.cuda.synchronize()
+    _check_guard(buf, M, K)
+    return dX.cpu().numpy()
+
+
+def run_dw(A, dY):
+    M, K = A.shape
+    N = dY.shape[1]
+    buf, dW = _guarded(K, N)
+    t3.t3_gemm_bwd_dw(_dev(A), _dev(dY), dW=dW)
+    torch.cuda.synchronize()
+    _check_guard(buf, K, N)
+    return dW.cpu().numpy()
+
+
+def assert_same(got, want, what):
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, (f"{what}: {len(bad)} mismatches of {got.size}; first at {bad[0].tolist()}: "
+                           f"got {got[tuple(bad[0])]}, want {want[tuple(bad[0])]}")
+
+
+def inputs(M, N, K, seed, p_zero=1.0 / 3.0):
+    g = t3_synth.rng(seed)
+    A = t3_synth.int8_uniform(g, (M, K))
+    w = t3_synth.ternary(g, (K, N), p_zero)
+    dY = t3_synth.int8_uniform(g, (M, N))
+    return A, w, dY
+
+
+# ------------------------------------------------------------ small, full ---
+
+def test_ragged_300x272x96_forward():
+    """The pages' ragged case: every guard path (K=96 makes the packed row
+    24 bytes, which TMA cannot stride, so the plain-load producer runs)."""
+    wl = t3_synth.BY_NAME["fwd_ragged_300x272x96"]
+    A, w, _ = t3_synth.make_inputs(wl)
+    assert_same(run_fwd(A, t3.t3_pack_ternary(w)), oracle.fwd(A, oracle.pack(w)), "fwd 300x272x96")
+
+
+SMALL = [(1, 1, 1), (1, 16, 16), (128, 128, 32), (5, 7, 3), (70, 33, 65), (129, 257, 64),
+         (256, 256, 128), (200, 300, 200), (33, 513, 130), (300, 272, 96), (130, 1000, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_small_shapes_all_three(M, N, K):
+    A, w, dY = inputs(M, N, K, seed=M * 7 + N * 3 + K)
+    wp_gpu, wp_ref = t3.t3_pack_ternary(w), oracle.pack(w)
+    assert_same(run_fwd(A, wp_gpu), oracle.fwd(A, wp_ref), f"fwd {M}x{N}x{K}")
+    assert_same(run_dx(dY, wp_gpu, K), oracle.dx(dY, wp_ref, K), f"dX {M}x{N}x{K}")
+    assert_same(run_dw(A, dY), oracle.dw(A, dY), f"dW {M}x{N}x{K}")
+
+
+def test_random_tiny_shapes():
+    g = np.random.default_rng(1234)
+    for it in range(12):
+        M, N, K = (int(x) for x in g.integers(1, 71, size=3))
+        A, w, dY = inputs(M, N, K, seed=5000 + it)
+        wp = t3.t3_pack_ternary(w)
+        assert_same(run_fwd(A, wp), oracle.fwd(A, wp), f"fwd {M}x{N}x{K}")
+        assert_same(run_dx(dY, wp, K), oracle.dx(dY, wp, K), f"dX {M}x{N}x{K}")
+        assert_same(run_dw(A, dY), oracle.dw(A, dY), f"dW {M}x{N}x{K}")
+
+
+def test_raw_codes_and_pad_bits():
+    """Random packed bytes: code 3 everywhere it lands and nonzero pad bits."""
+    g = t3_synth.rng(77)
+    for (M, N, K) in [(9, 40, 13), (150, 260, 255), (64, 300, 1030)]:
+        wp = t3_synth.raw_bytes(g, (N, (K + 3) // 4))
+        A = t3_synth.int8_uniform(g, (M, K))
+        dY = t3_synth.int8_uniform(g, (M, N))
+        assert_same(run_fwd(A, wp), oracle.fwd(A, wp), f"fwd raw {M}x{N}x{K}")
+        assert_same(run_dx(dY, wp, K), oracle.dx(dY, wp, K), f"dX raw {M}x{N}x{K}")
+
+
+def test_unaligned_pointers_take_plain_load_path():
+    """Operands at odd byte offsets cannot be TMA sources; results are the same."""
+    M, N, K = 150, 200, 320
+    A, w, dY = inputs(M, N, K, seed=99)
+    wp = t3.t3_pack_ternary(w)
+    def shifted(a):
+        flat = np.ascontiguousarray(a).reshape(-1)
+        buf = torch.empty(flat.size + 1, dtype=torch.from_numpy(flat).dtype, device="cuda")
+        buf[1:] = torch.from_numpy(flat).cuda()
+        return buf[1:].view(a.shape)
+    C = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    t3.t3_gemm_fwd(shifted(A), shifted(wp), K=K, C=C)
+    assert_same(C.cpu().numpy(), oracle.fwd(A, wp), "fwd unaligned")
+    dX = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    t3.t3_gemm_bwd_dx(shifted(dY), shifted(wp), K, dX=dX)
+    assert_same(dX.cpu().numpy(), oracle.dx(dY, wp, K), "dX unaligned")
+    dW = torch.empty((K, N), dtype=torch.int32, device="cuda")
+    t3.t3_gemm_bwd_dw(shifted(A), shifted(dY), dW=dW)
+    assert_same(dW.cpu().numpy(), oracle.dw(A, dY), "dW unaligned")
+
+
+# ------------------------------------------------------ exactness extremes --
+
+def test_int32_extremes_and_long_reductions():
+    # 128 * K at K = 8192
+    K, M, N = 8192, 130, 300
+    A = np.full((M, K), -128, dtype=np.int8)
+    wp = t3.t3_pack_ternary(-np.ones((K, N), dtype=np.int8))
+    C = run_fwd(A, wp)
+    assert np.all(C == 128 * K)
+    # dW over 1782 rows at the extreme: 16384 * 1782 > 2^24, so the f32
+    # accumulator alone could not hold it exactly; the chunked sum must.
+    M2 = 1782
+    A2 = np.full((M2, 96), -128, dtype=np.int8)
+    dW = run_dw(A2, A2[:, :80].copy())
+    assert np.all(dW == 16384 * M2)
+
+
+def test_adversarial_large_then_small_terms():
+    """A large running sum followed by +-1 terms: any loss of low bits in the
+    f32 accumulation shows up as a mismatch."""
+    g = t3_synth.rng(31)
+    M, N, K = 256, 256, 4096
+    A = np.empty((M, K), dtype=np.int8)
+    A[:, : K // 2] = 127
+    A[:, K // 2:] = g.choice(np.array([-1, 1], dtype=np.int8), size=(M, K - K // 2))
+    w = t3_synth.ternary(g, (K, N), 0.0)
+    w[: K // 2] = 1
+    wp = t3.t3_pack_ternary(w)
+    assert_same(run_fwd(A, wp), oracle.fwd(A, oracle.pack(w)), "fwd adversarial")
+    # dW: rows of 127*127 products then +-1 products, across the chunk boundary
+    M3 = 1500
+    A3 = np.empty((M3, 64), dtype=np.int8)
+    A3[:1000] = 127
+    A3[1000:] = g.choice(np.array([-1, 1], dtype=np.int8), size=(M3 - 1000, 64))
+    dY3 = A3[:, ::-1].copy()
+    assert_same(run_dw(A3, dY3), oracle.dw(A3, dY3), "dW adversarial")
+
+
+# ------------------------------------------------------- full-size, sampled -
+
+def sample_rows(total, n, seed):
+    g = np.random.default_rng(seed)
+    rows = set(g.choice(total, size=min(n, total), replace=False).tolist())
+    rows.update({0, total - 1})
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["fwd_square_4096", "fwd_16384x3456x1280"])
+def test_full_size_forward_sampled(name):
+    wl = t3_synth.BY_NAME[name]
+    A, w, _ = workload_inputs(name)
+    wp = t3.t3_pack_ternary(w)
+    C = torch.empty((wl.M, wl.N), dtype=torch.int32, device="cuda")
+    t3.t3_gemm_fwd(_dev(A), _dev(wp), K=wl.K, C=C)
+    rows = sample_rows(wl.M, 48, wl.seed)
+    got = C[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_same(got, oracle.fwd(A, oracle.pack(w), rows), name)
+
+
+@pytest.mark.parametrize("M", [1782, 16384])
+def test_full_size_backward_sampled(M):
+    N, K = 3456, 1280
+    wl = t3_synth.BY_NAME["bwd_1782x3456x1280"]
+    A, w, dY = (t3_synth.make_inputs(wl) if M == wl.M else inputs(M, N, K, seed=2))
+    wp = t3.t3_pack_ternary(w)
+    dX = t3.t3_gemm_bwd_dx(_dev(dY), _dev(wp), K)
+    dW = t3.t3_gemm_bwd_dw(_dev(A), _dev(dY))
+    rows = sample_rows(M, 24, 3)
+    got = dX[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_same(got, oracle.dx(dY, oracle.pack(w), K, rows), f"dX M={M}")
+    krows = sample_rows(K, 12, 4)
+    got = dW[torch.from_numpy(krows).cuda()].cpu().numpy()
+    assert_same(got, oracle.dw(A, dY, krows), f"dW M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 8, 27])
+@pytest.mark.parametrize("NK", [(3456, 1280), (8192, 8192)])
+def test_small_m_forward(M, NK):
+    N, K = NK
+    wl = t3_synth.BY_NAME[f"skinny_m{M}_n{N}_k{K}"]
+    A, w, _ = workload_inputs(wl.name)
+    wp = t3.t3_pack_ternary(w)
+    C = run_fwd(A, wp)
+    rows = np.arange(M) if N * K * M <= 3456 * 1280 * 27 else sample_rows(M, 3, 5)
+    assert_same(C[rows], oracle.fwd(A, oracle.pack(w), rows), wl.name)
+
+
+def test_repeated_calls_same_result():
+    A, w, dY = inputs(300, 600, 700, seed=8)
+    wp = t3.t3_pack_ternary(w)
+    first = run_fwd(A, wp)
+    for _ in range(3):
+        assert np.array_equal(run_fwd(A, wp), first)
+
+
+def test_empty_reduction_writes_zeros():
+    C = torch.full((5, 7), 3, dtype=torch.int32, device="cuda")
+    t3.t3_gemm_fwd(torch.empty((5, 0), dtype=torch.int8, device="cuda"),
+                   torch.empty((7, 0), dtype=torch.uint8, device="cuda"), K=0, C=C)
+    assert torch.count_nonzero(C).item() == 0
