@@ -19,7 +19,7 @@ import ternary_weight_int8_t3_gb300 as t3
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-CANARY = 0x5A5A5A5A - (1 << 32)  # an int32 no product here can produce by accident
+CANARY = 0x5A5A5A5A  # an int32 value that marks untouched words
 PAD = 64                         # canary words on each side of an output
 
 
