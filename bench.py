@@ -1,0 +1,369 @@
+"""Benchmark of the ternary-weight x int8 layer step on GB300.
+
+One step = the three products of one ternary layer at M=16384 rows, N=3456,
+K=1280 (the pages' largest forward shape, with the two backward products at
+the same shape):
+    C  = A . W        t3_gemm_fwd     (int8 x ternary -> int32)
+    dX = dY . W^T     t3_gemm_bwd_dx  (int8 x ternary -> int32)
+    dW = A^T . dY     t3_gemm_bwd_dw  (int8 x int8    -> int32)
+The metric counts 2*M*N*K operations per product (zeros included), as the
+pages do.  Inputs are synthetic and seeded (t3_synth), resident in HBM before
+the timed region; the step moves ~410 MB, far more than the 129 MB L2, so no
+explicit L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain int64 loops) on a bounded
+sample of rows of the same workload, on the host cores.
+Multi-GPU runs (torchrun) are independent replicas: the products have no
+exchange step on one layer, so nothing is communicated on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import t3_synth  # noqa: E402
+
+METRIC = "TOPS (2·M·N·K/s) ternary×int8 fwd/dX/dW; % of int8 tensor peak / HBM roofline"
+UNIT = "TOPS"
+M, N, K = 16384, 3456, 1280
+SEED = 2
+OPS_PER_PRODUCT = 2 * M * N * K
+WORKLOAD = f"ternary layer step fwd+dX+dW, M={M} N={N} K={K}"
+FALLBACK_TFLOPS = 1900.0
+PAGES_CONTEXT = "pages: fwd 16384x3456x1280 at 171 TOPS on an RTX 4090 (other hardware, fwd only)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def make_host_inputs():
+    g = t3_synth.rng(SEED)
+    A = t3_synth.int8_uniform(g, (M, K))
+    w = t3_synth.ternary(g, (K, N))
+    dY = t3_synth.int8_uniform(g, (M, N))
+    return A, w, dY
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {}, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(A, w, dY, target_s=12.0):
+    """The oracle, as it stands, on a bounded sample of rows of each product."""
+    import oracle
+    wp = oracle.pack(w)
+    total_ops, total_t, sample = 0, 0.0, []
+    per_op = target_s / 3.0
+    for name in ("fwd", "dx", "dw"):
+        rows_probe = 4
+        def run(nrows):
+            rows = np.linspace(0, (M if name != "dw" else K) - 1, nrows).astype(np.int64)
+            t0 = time.perf_counter()
+            if name == "fwd":
+                oracle.fwd(A, wp, rows)
+                ops = 2 * nrows * N * K
+            elif name == "dx":
+                oracle.dx(dY, wp, K, rows)
+                ops = 2 * nrows * N * K
+            else:
+                oracle.dw(A, dY, rows)
+                ops = 2 * nrows * N * M
+            return ops, time.perf_counter() - t0
+        ops, t = run(rows_probe)
+        nrows = max(rows_probe, int(rows_probe * per_op / max(t, 1e-3)))
+        nrows = min(nrows, M if name != "dw" else K)
+        ops, t = run(nrows)
+        total_ops += ops
+        total_t += t
+        sample.append(f"{name}: {nrows} output rows")
+    return {"value": total_ops / total_t / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": "; ".join(sample) + f" of the {WORKLOAD} ({total_t:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step a bounded row sample."""
+    if rank != 0:
+        return
+    import oracle
+    A, w, dY = make_host_inputs()
+    wp = oracle.pack(w)
+    rows_fwd = np.linspace(0, M - 1, 6).astype(np.int64)
+    rows_dw = np.linspace(0, K - 1, 6).astype(np.int64)
+    ops_step = 2 * len(rows_fwd) * N * K * 2 + 2 * len(rows_dw) * N * M
+
+    def step():
+        oracle.fwd(A, wp, rows_fwd)
+        oracle.dx(dY, wp, K, rows_fwd)
+        oracle.dw(A, dY, rows_dw)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = ops_step * args.steps / el / 1e12
+    sample = (f"per step: fwd and dX on {len(rows_fwd)} rows each, dW on {len(rows_dw)} rows, "
+              f"of the {WORKLOAD}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import ternary_weight_int8_t3_gb300 as t3
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    A, w, dY = make_host_inputs()
+    wp = t3.t3_pack_ternary(w)
+    A_d = torch.from_numpy(A).to(dev)
+    wp_d = torch.from_numpy(wp).to(dev)
+    dY_d = torch.from_numpy(dY).to(dev)
+    C = torch.empty((M, N), dtype=torch.int32, device=dev)
+    dX = torch.empty((M, K), dtype=torch.int32, device=dev)
+    dW = torch.empty((K, N), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        t3.t3_gemm_fwd(A_d, wp_d, K=K, C=C, stream=stream)
+        t3.t3_gemm_bwd_dx(dY_d, wp_d, K, dX=dX, stream=stream)
+        t3.t3_gemm_bwd_dw(A_d, dY_d, dW=dW, stream=stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    barrier()
+
+    # ---- device-resident timed region, per-product events on the launch stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            e = ev[i]
+            e[0].record(stream)
+            t3.t3_gemm_fwd(A_d, wp_d, K=K, C=C, stream=stream)
+            e[1].record(stream)
+            t3.t3_gemm_bwd_dx(dY_d, wp_d, K, dX=dX, stream=stream)
+            e[2].record(stream)
+            t3.t3_gemm_bwd_dw(A_d, dY_d, dW=dW, stream=stream)
+            e[3].record(stream)
+        stop.record(stream)
+        barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    per = {"fwd": [], "dx": [], "dw": []}
+    for e in ev:
+        per["fwd"].append(e[0].elapsed_time(e[1]))
+        per["dx"].append(e[1].elapsed_time(e[2]))
+        per["dw"].append(e[2].elapsed_time(e[3]))
+    rc, detail = t3.t3_last_device_error()
+    if rc != t3.T3_OK:
+        raise RuntimeError(f"device wait timed out during the bench ({detail:#x})")
+
+    elapsed_max = elapsed_ms
+    if pg is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_max = float(t.item())
+
+    # ---- end to end: pinned host inputs in, results out, every step
+    A_h = torch.from_numpy(A).pin_memory()
+    wp_h = torch.from_numpy(wp).pin_memory()
+    dY_h = torch.from_numpy(dY).pin_memory()
+    C_h = torch.empty((M, N), dtype=torch.int32).pin_memory()
+    dX_h = torch.empty((M, K), dtype=torch.int32).pin_memory()
+    dW_h = torch.empty((K, N), dtype=torch.int32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        A_d.copy_(A_h, non_blocking=True)
+        wp_d.copy_(wp_h, non_blocking=True)
+        dY_d.copy_(dY_h, non_blocking=True)
+        step()
+        C_h.copy_(C, non_blocking=True)
+        dX_h.copy_(dX, non_blocking=True)
+        dW_h.copy_(dW, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    s2, t2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    t2.record(stream)
+    barrier()
+    e2e_ms = s2.elapsed_time(t2) / e2e_steps
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = A.nbytes + wp.nbytes + dY.nbytes
+    d2h = (M * N + M * K + K * N) * 4
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+
+    ms_step = elapsed_max / args.steps
+    value = 3 * OPS_PER_PRODUCT * world / (ms_step * 1e-3) / 1e12
+    avg = {k: sum(v) / len(v) for k, v in per.items()}
+    op_tops = {k: OPS_PER_PRODUCT / (avg[k] * 1e-3) / 1e12 for k in avg}
+    dominant = max(avg, key=avg.get)
+    peaks, peak_src = read_peaks()
+    long_region = elapsed_ms > 1000.0
+    if peak_src == "measured":
+        peak = peaks.get("bf16_tflops_sustained" if long_region else "bf16_tflops", FALLBACK_TFLOPS)
+        peak_note = ("sustained" if long_region else "burst") + " bf16 dense of measured; f16 runs at the bf16 rate"
+    else:
+        peak, peak_note = FALLBACK_TFLOPS, "bf16 dense of fallback; f16 runs at the bf16 rate"
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            traffic = json.load(f).get(dominant)
+    kname = {"fwd": "t3_gemm_fwd", "dx": "t3_gemm_bwd_dx", "dw": "t3_gemm_bwd_dw"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "seed": SEED,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "arith": "int8 x ternary (and int8 x int8) -> exact int32 via f16 tcgen05 operands, f32 TMEM accumulation",
+                   "l2": "per-step traffic ~410 MB > 129 MB L2; no flush",
+                   "context": PAGES_CONTEXT},
+        "per_product_tops": op_tops,
+        "per_product_ms": avg,
+        "roofline": {"kernel": kname[dominant], "bound": "tensor", "achieved": op_tops[dominant],
+                     "peak": peak, "unit": "TFLOP/s", "frac": op_tops[dominant] / peak,
+                     "traffic": traffic, "peak_source": peak_note},
+        "gpu_launches": 3 * args.steps,
+        "e2e": {"value": 3 * OPS_PER_PRODUCT * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(A, w, dY)
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
