@@ -50,10 +50,12 @@ constexpr int RAW_STAGES = 4;
 constexpr int OP_STAGES = 2;
 constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kEpiWarp0 = 6;
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kProducerWarp = kConvWarps;
+constexpr int kMmaWarp = kConvWarps + 1;
+constexpr int kEpiWarp0 = kConvWarps + 2;
+constexpr int kThreads = 32 * (kConvWarps + 2 + 4);
 constexpr int OPA_BYTES = BM * BK * 2;
 constexpr int OPB_BYTES = BN * BK * 2;
 
@@ -191,8 +193,8 @@ __device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r &
 // int8 rows [128][64] (reduction contiguous) -> f16 rows [128][64].
 __device__ __forceinline__ void convert_rows_s8(const uint8_t* raw, uint8_t* op, int tid) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int u = tid + 128 * i, r = u >> 2, c = u & 3;
+  for (int i = 0; i < 512 / kConvThreads; ++i) {
+    const int u = tid + kConvThreads * i, r = u >> 2, c = u & 3;
     const uint4 x = *reinterpret_cast<const uint4*>(raw + r * 64 + c * 16);
     uint4 o0, o1;
     s8x4_to_f16(x.x, o0.x, o0.y);
@@ -208,8 +210,8 @@ __device__ __forceinline__ void convert_rows_s8(const uint8_t* raw, uint8_t* op,
 // rows [256 n][64 k].
 __device__ __forceinline__ void decode_rows_w(const uint8_t* raw, uint8_t* op, int tid) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int u = tid + 128 * i, r = u >> 2, w = u & 3;
+  for (int i = 0; i < 1024 / kConvThreads; ++i) {
+    const int u = tid + kConvThreads * i, r = u >> 2, w = u & 3;
     const uint32_t x = *reinterpret_cast<const uint32_t*>(raw + r * 16 + w * 4);
     *reinterpret_cast<uint4*>(op + sw128(r, 2 * w)) =
         decode8_nibbles(spread_codes_to_nibbles(x & 0xFFFFu));
@@ -219,11 +221,13 @@ __device__ __forceinline__ void decode_rows_w(const uint8_t* raw, uint8_t* op, i
 }
 
 // dX weights: packed [64 n][64 bytes = 256 codes along k] -> f16 rows
-// [256 k][64 n]: a transposing decode.  Thread = (word column w, group of 8
-// n-rows g); g is rotated by w so that each 8-thread store phase hits 8
-// distinct bank groups.
+// [256 k][64 n]: a transposing decode.  Unit = (word column w, group of 8
+// n-rows g), split across kConvThreads/128 threads by byte b; g is rotated by
+// w so that each 8-thread store phase hits 8 distinct bank groups.
 __device__ __forceinline__ void decode_cols_w(const uint8_t* raw, uint8_t* op, int tid) {
-  const int w = tid & 15, g = ((tid >> 4) + w) & 7;
+  constexpr int kParts = kConvThreads / 128, kBytes = 4 / kParts;
+  const int t = tid & 127, part = tid >> 7;
+  const int w = t & 15, g = ((t >> 4) + w) & 7;
   const uint32_t* rw = reinterpret_cast<const uint32_t*>(raw);
   uint32_t x[8];
 #pragma unroll
@@ -233,6 +237,7 @@ __device__ __forceinline__ void decode_cols_w(const uint8_t* raw, uint8_t* op, i
   transpose4x4(x[4], x[5], x[6], x[7], Z);
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
+    if (b / kBytes != part) continue;  // warp-uniform; keeps Y[b] statically indexed
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int krow = 16 * w + 4 * b + j;
@@ -251,11 +256,12 @@ __device__ __forceinline__ void decode_cols_w(const uint8_t* raw, uint8_t* op, i
 // f16 rows [ROW_WORDS*4][64 m]: a transposing conversion.
 template <int ROW_WORDS>
 __device__ __forceinline__ void convert_cols_s8(const uint8_t* raw, uint8_t* op, int tid) {
-  constexpr int kUnits = ROW_WORDS * 8 / 128;
+  constexpr int kUnits = ROW_WORDS * 8 / kConvThreads;
+  static_assert(kUnits >= 1, "one unit per thread at least");
   const uint32_t* rw = reinterpret_cast<const uint32_t*>(raw);
 #pragma unroll
   for (int i = 0; i < kUnits; ++i) {
-    const int u = tid + 128 * i, w = u % ROW_WORDS, g = ((u / ROW_WORDS) + w) & 7;
+    const int u = tid + kConvThreads * i, w = u % ROW_WORDS, g = ((u / ROW_WORDS) + w) & 7;
     uint32_t x[8];
 #pragma unroll
     for (int ii = 0; ii < 8; ++ii) x[ii] = rw[(8 * g + ii) * ROW_WORDS + w];
@@ -355,10 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RAW_STAGES; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 4);
+      mbar_init(&raw_empty[s], kConvWarps);
     }
     for (int s = 0; s < OP_STAGES; ++s) {
-      mbar_init(&op_full[s], 4);
+      mbar_init(&op_full[s], kConvWarps);
       mbar_init(&op_empty[s], 1);
     }
     for (int s = 0; s < ACC_BUFS; ++s) {
@@ -378,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  if (warp < 4) {
+  if (warp < kConvWarps) {
     // ---------------------------------------------------------- converters
     const int tid = threadIdx.x;
     uint32_t rs = 0, rph = 0, os = 0, oph = 0;
