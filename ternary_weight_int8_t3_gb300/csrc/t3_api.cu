@@ -6,7 +6,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/t3.h"
+#include "t3.h"
 #include "t3_internal.h"
 
 namespace t3 {
@@ -91,6 +91,23 @@ bool make_u8_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
   return r == CUDA_SUCCESS;
 }
 
+// Describes the int32 output [rows][cols] for bulk stores of 128 x 32 boxes
+// staged in the 128-byte swizzle layout.  False when TMA cannot be used.
+bool make_i32_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+  std::memset(map, 0, sizeof(*map));
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (cols * 4) % 16 != 0) return false;
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 4)};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(tc::BM)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 template <int OP>
@@ -121,14 +138,15 @@ int run_tc(const uint8_t* a_src, int64_t a_rows, int64_t a_cols, const uint8_t* 
   p.tiles_c = static_cast<int>(tiles_c);
   p.err = dev->err_word;
   p.op_code = OP;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mo;
   p.use_tma_a = make_u8_map(&ma, a_src, a_rows, a_cols, a_cols, R::a_rows, R::a_cols) ? 1 : 0;
   p.use_tma_b = make_u8_map(&mb, b_src, b_rows, b_cols, b_cols, R::b_rows, R::b_cols) ? 1 : 0;
+  p.use_tma_out = make_i32_out_map(&mo, out, out_rows, out_cols) ? 1 : 0;
   const int64_t tiles = tiles_r * tiles_c;
   const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
-  if (OP == kOpFwd) return launch_tc_fwd(p, ma, mb, grid, stream);
-  if (OP == kOpDx) return launch_tc_dx(p, ma, mb, grid, stream);
-  return launch_tc_dw(p, ma, mb, grid, stream);
+  if (OP == kOpFwd) return launch_tc_fwd(p, ma, mb, mo, grid, stream);
+  if (OP == kOpDx) return launch_tc_dx(p, ma, mb, mo, grid, stream);
+  return launch_tc_dw(p, ma, mb, mo, grid, stream);
 }
 
 bool bad_dims(int64_t M, int64_t N, int64_t K) {

@@ -1,12 +1,12 @@
 // t3_tc_dw.cu -- instantiates the tensor-core pipeline for one product.
 #include <atomic>
 #include "t3_internal.h"
-#include "../../include/t3.h"
+#include "t3.h"
 
 namespace t3 {
 
-int launch_tc_dw(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap& mb, int grid,
-                  cudaStream_t s) {
+int launch_tc_dw(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap& mb,
+                  const CUtensorMap& mo, int grid, cudaStream_t s) {
   constexpr int kSmem = tc::Layout<kOpDw>::smem_alloc;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
@@ -18,7 +18,7 @@ int launch_tc_dw(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap& 
       return T3_ECUDA;
     attr_done[dev].store(true, std::memory_order_release);
   }
-  tc::tc_gemm_kernel<kOpDw><<<grid, tc::kThreads, kSmem, s>>>(p, ma, mb);
+  tc::tc_gemm_kernel<kOpDw><<<grid, tc::kThreads, kSmem, s>>>(p, ma, mb, mo);
   return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
 }
 

@@ -46,7 +46,8 @@ constexpr int BM = 128;  // output rows per tile (TMEM lanes)
 constexpr int BN = 256;  // output columns per tile (MMA N)
 constexpr int BK = 64;   // reduction elements per pipeline stage (128 B of f16)
 constexpr int UK = 16;   // reduction elements per tcgen05.mma (kind::f16)
-constexpr int RAW_STAGES = 4;
+// Raw stages in flight: enough bytes to cover L2/HBM latency at the MMA rate.
+template <int OP> struct RawStages { static constexpr int value = 6; };
 constexpr int OP_STAGES = 2;
 constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512
@@ -75,14 +76,23 @@ template <> struct Raw<kOpDw> {   // A [BK m][BM k];  dY [BK m][BN n]
   static constexpr int a_rows = BK, a_cols = BM, b_rows = BK, b_cols = BN;
 };
 
+template <> struct RawStages<kOpDw> { static constexpr int value = 3; };
+
+// Output staging for the bulk-store epilogue: two [128 rows][32 int32]
+// buffers in the 128-byte swizzle layout.
+constexpr int STAGE_OUT_BYTES = BM * 32 * 4;
+constexpr int kEpiBarrier = 1;  // named barrier of the 4 epilogue warps
+
 template <int OP> struct Layout {
+  static constexpr int RAW_STAGES = RawStages<OP>::value;
   static constexpr int raw_a = Raw<OP>::a_rows * Raw<OP>::a_cols;
   static constexpr int raw_b = Raw<OP>::b_rows * Raw<OP>::b_cols;
   static constexpr int raw_stage = raw_a + raw_b;
   static constexpr int off_opa = 0;
   static constexpr int off_opb = off_opa + OP_STAGES * OPA_BYTES;
   static constexpr int off_raw = off_opb + OP_STAGES * OPB_BYTES;
-  static constexpr int off_bar = off_raw + RAW_STAGES * raw_stage;
+  static constexpr int off_out = off_raw + RAW_STAGES * raw_stage;
+  static constexpr int off_bar = off_out + 2 * STAGE_OUT_BYTES;
   static constexpr int n_bars = 2 * RAW_STAGES + 2 * OP_STAGES + 2 * ACC_BUFS + 1;
   static constexpr int off_misc = off_bar + 8 * n_bars;
   static constexpr int bytes = off_misc + 16;
@@ -100,6 +110,7 @@ struct Params {
   int64_t chunk_kb;  // stages per exact f32 chunk
   int tiles_r, tiles_c;
   int use_tma_a, use_tma_b;
+  int use_tma_out;  // output written with bulk tensor stores (needs out_cols % 4 == 0)
   int* err;  // device error word
   int op_code;
 };
@@ -333,7 +344,8 @@ __device__ __forceinline__ void store_row32(int32_t* dst, const uint32_t (&v)[32
 template <int OP>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const Params p, const __grid_constant__ CUtensorMap map_a,
-                   const __grid_constant__ CUtensorMap map_b) {
+                   const __grid_constant__ CUtensorMap map_b,
+                   const __grid_constant__ CUtensorMap map_out) {
   using L = Layout<OP>;
   using R = Raw<OP>;
   extern __shared__ uint8_t smem_raw[];
@@ -343,8 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* opa = smem + L::off_opa;
   uint8_t* opb = smem + L::off_opb;
   uint8_t* raw = smem + L::off_raw;
+  uint8_t* stage_out = smem + L::off_out;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
   uint64_t* raw_full = bars;
+  constexpr int RAW_STAGES = L::RAW_STAGES;
   uint64_t* raw_empty = raw_full + RAW_STAGES;
   uint64_t* op_full = raw_empty + RAW_STAGES;
   uint64_t* op_empty = op_full + OP_STAGES;
@@ -506,17 +520,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ----------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int epi_tid = threadIdx.x - kEpiWarp0 * 32;
     const bool vec_ok = (p.out_cols % 4 == 0) &&
                         (reinterpret_cast<uintptr_t>(p.out) % 16 == 0);
-    uint32_t ab = 0, aph = 0;
+    const int srow = q * 32 + lane;  // staging row = TMEM lane = tile row
+    uint32_t ab = 0, aph = 0, slab = 0;
     bool ok = true;
+    if (p.use_tma_out && epi_tid == 0) prefetch_tensormap(&map_out);
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
       const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
-      const int64_t row = static_cast<int64_t>(tr) * BM + q * 32 + lane;
+      const int64_t row = static_cast<int64_t>(tr) * BM + srow;
       for (int64_t c0 = 0; c0 < p.num_kb; c0 += p.chunk_kb) {
         ok = mbar_wait(&acc_full[ab], aph, abort_flag, p.err, code_base | 4);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        // One decision for all four epilogue warps: they share named barriers below.
+        ok = named_bar_and(kEpiBarrier, 128, __all_sync(0xffffffffu, ok));
+        if (!ok) break;
         tc_fence_after();
+        const bool first = (c0 == 0);
+        // A later chunk adds into what the first one stored: let those
+        // stores land before the first add is issued.
+        if (p.use_tma_out && c0 == p.chunk_kb && epi_tid == 0) bulk_wait_group<0>();
         for (int cb = 0; cb < BN / 32; ++cb) {
           const int64_t col0 = static_cast<int64_t>(tcol) * BN + cb * 32;
           if (col0 >= p.out_cols) break;
@@ -524,10 +547,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * BN + cb * 32,
                              v);
           tmem_wait_ld();
-          if (row < p.out_rows) {
+          if (p.use_tma_out) {
+            uint8_t* buf = stage_out + (slab & 1) * STAGE_OUT_BYTES;
+            if (epi_tid == 0) bulk_wait_group_read<1>();  // the store 2 slabs ago has read buf
+            named_bar_sync(kEpiBarrier, 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int4 val = make_int4(f32_bits_to_i32(v[4 * c]), f32_bits_to_i32(v[4 * c + 1]),
+                                         f32_bits_to_i32(v[4 * c + 2]),
+                                         f32_bits_to_i32(v[4 * c + 3]));
+              *reinterpret_cast<int4*>(buf + sw128(srow, c)) = val;
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(kEpiBarrier, 128);
+            if (epi_tid == 0) {
+              if (first)
+                tma_store_2d(&map_out, buf, static_cast<int>(col0), tr * BM);
+              else
+                tma_reduce_add_2d(&map_out, buf, static_cast<int>(col0), tr * BM);
+              bulk_commit_group();
+            }
+            ++slab;
+          } else if (row < p.out_rows) {
             const int64_t rem = p.out_cols - col0;
             store_row32(p.out + row * p.out_cols + col0, v, rem < 32 ? static_cast<int>(rem) : 32,
-                        c0 == 0, vec_ok);
+                        first, vec_ok);
           }
         }
         tc_fence_before();
@@ -536,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++ab == ACC_BUFS) { ab = 0; aph ^= 1u; }
       }
     }
+    if (p.use_tma_out && epi_tid == 0) bulk_wait_group<0>();
   }
 
   tc_fence_before();
