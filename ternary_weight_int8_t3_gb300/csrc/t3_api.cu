@@ -16,12 +16,63 @@ namespace t3 {
 // and clears it.
 __device__ int g_error_word;
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+
+bool make_u8_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                       int box_rows, int box_cols) {
+  std::memset(map, 0, sizeof(*map));
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || ld % 16 != 0) return false;
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) std::memset(map, 0, sizeof(*map));
+  return r == CUDA_SUCCESS;
+}
+
+bool make_i32_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                        int box_rows, int box_cols, bool swizzle128) {
+  std::memset(map, 0, sizeof(*map));
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (cols * 4) % 16 != 0) return false;
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 4)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) std::memset(map, 0, sizeof(*map));
+  return r == CUDA_SUCCESS;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = 2147483647LL;           // TMA coordinates are int32
 constexpr int64_t kMaxTernaryReduction = 16777215;  // 128 * K <= INT32_MAX
 constexpr int64_t kMaxInt8Reduction = 131071;       // 16384 * M <= INT32_MAX
+constexpr int64_t kSmallM = 32;                     // forward rows served by the small-M path
 
 struct DeviceInfo {
   bool ready = false;
@@ -57,57 +108,6 @@ int device_info(const DeviceInfo** out) {
   return d.status;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// Describes a row-major byte matrix [rows][cols] (row stride ld) for 2-D TMA
-// boxes of box_rows x box_cols.  Returns false when TMA cannot be used (base
-// or stride not 16-byte aligned, or the driver refuses); the kernel then
-// loads that operand with plain loads.
-bool make_u8_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
-                 int box_rows, int box_cols) {
-  std::memset(map, 0, sizeof(*map));
-  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || ld % 16 != 0) return false;
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// Describes the int32 output [rows][cols] for bulk stores of 128 x 32 boxes
-// staged in the 128-byte swizzle layout.  False when TMA cannot be used.
-bool make_i32_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
-  std::memset(map, 0, sizeof(*map));
-  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (cols * 4) % 16 != 0) return false;
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 4)};
-  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(tc::BM)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 template <int OP>
@@ -139,9 +139,9 @@ int run_tc(const uint8_t* a_src, int64_t a_rows, int64_t a_cols, const uint8_t* 
   p.err = dev->err_word;
   p.op_code = OP;
   CUtensorMap ma, mb, mo;
-  p.use_tma_a = make_u8_map(&ma, a_src, a_rows, a_cols, a_cols, R::a_rows, R::a_cols) ? 1 : 0;
-  p.use_tma_b = make_u8_map(&mb, b_src, b_rows, b_cols, b_cols, R::b_rows, R::b_cols) ? 1 : 0;
-  p.use_tma_out = make_i32_out_map(&mo, out, out_rows, out_cols) ? 1 : 0;
+  p.use_tma_a = make_u8_map_tiled(&ma, a_src, a_rows, a_cols, a_cols, R::a_rows, R::a_cols) ? 1 : 0;
+  p.use_tma_b = make_u8_map_tiled(&mb, b_src, b_rows, b_cols, b_cols, R::b_rows, R::b_cols) ? 1 : 0;
+  p.use_tma_out = make_i32_map_tiled(&mo, out, out_rows, out_cols, tc::BM, 32, true) ? 1 : 0;
   const int64_t tiles = tiles_r * tiles_c;
   const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
   if (OP == kOpFwd) return launch_tc_fwd(p, ma, mb, mo, grid, stream);
@@ -201,6 +201,12 @@ int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64
   if (!A || !Wp || !C) return T3_EINVAL;
   if (K > kMaxTernaryReduction) return T3_EOVERFLOW;
   const int64_t KB = (K + 3) / 4;
+  if (M <= kSmallM) {
+    const DeviceInfo* dev = nullptr;
+    int st = device_info(&dev);
+    if (st != T3_OK) return st;
+    return launch_skinny_fwd(A, Wp, C, M, N, K, dev->sms, dev->err_word, stream);
+  }
   return run_tc<kOpFwd>(reinterpret_cast<const uint8_t*>(A), M, K, Wp, N, KB, C, M, N, K,
                         tc::kChunkKbTernary, stream);
 }

@@ -15,4 +15,16 @@ int launch_tc_dx(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap& 
 int launch_tc_dw(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap& mb,
                   const CUtensorMap& mo, int grid, cudaStream_t s);
 
+// Tensor maps for 2-D row-major matrices (row stride = cols elements).  They
+// return false, leaving *map zeroed, when TMA cannot be used (base or row
+// stride not 16-byte aligned, or the driver refuses).
+bool make_u8_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                       int box_rows, int box_cols);
+bool make_i32_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                        int box_rows, int box_cols, bool swizzle128);
+
+// Small-M forward (M <= 32): zeroes C on `s`, then accumulates into it.
+int launch_skinny_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,
+                      int64_t K, int sms, int* err, cudaStream_t s);
+
 }  // namespace t3

@@ -250,6 +250,24 @@ def test_small_m_forward(M, NK):
     assert_same(C[rows], oracle.fwd(A, oracle.pack(w), rows), wl.name)
 
 
+@pytest.mark.parametrize("M", [1, 2, 15, 16, 17, 31, 32, 33])
+def test_small_m_boundaries(M):
+    """Rows on both sides of the small-M path's limits (16 and 32 rows), with
+    several k-groups, TMA and plain-load weight paths, bulk and atomic outputs."""
+    for (N, K) in [(300, 1100), (1024, 2048), (130, 2500), (256, 64)]:
+        A, w, _ = inputs(M, N, K, seed=M * 13 + N + K)
+        wp = t3.t3_pack_ternary(w)
+        assert_same(run_fwd(A, wp), oracle.fwd(A, oracle.pack(w)), f"fwd {M}x{N}x{K}")
+
+
+def test_small_m_extremes():
+    K = 8192
+    for M in (1, 27):
+        A = np.full((M, K), -128, dtype=np.int8)
+        wp = t3.t3_pack_ternary(-np.ones((K, 200), dtype=np.int8))
+        assert np.all(run_fwd(A, wp) == 128 * K)
+
+
 def test_repeated_calls_same_result():
     A, w, dY = inputs(300, 600, 700, seed=8)
     wp = t3.t3_pack_ternary(w)
