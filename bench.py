@@ -173,14 +173,14 @@ def bench_small_m(t3, torch, dev, stream, hbm_gbs, reps=30):
     return out
 
 
-def cpu_baseline(A, w, dY, target_s=12.0):
+def cpu_baseline(A, w, dY, target_s=15.0):
     """The oracle, as it stands, on a bounded sample of rows of each product."""
     import oracle
     wp = oracle.pack(w)
     total_ops, total_t, sample = 0, 0.0, []
     per_op = target_s / 3.0
     for name in ("fwd", "dx", "dw"):
-        rows_probe = 4
+        rows_probe = 32 if name != "dw" else 4
         def run(nrows):
             rows = np.linspace(0, (M if name != "dw" else K) - 1, nrows).astype(np.int64)
             t0 = time.perf_counter()
@@ -195,7 +195,7 @@ def cpu_baseline(A, w, dY, target_s=12.0):
                 ops = 2 * nrows * N * M
             return ops, time.perf_counter() - t0
         ops, t = run(rows_probe)
-        nrows = max(rows_probe, int(rows_probe * per_op / max(t, 1e-3)))
+        nrows = max(rows_probe, int(rows_probe * per_op / max(t, 1e-4)))
         nrows = min(nrows, M if name != "dw" else K)
         ops, t = run(nrows)
         total_ops += ops
