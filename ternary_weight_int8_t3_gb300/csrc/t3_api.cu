@@ -2,6 +2,7 @@
 // launches and the device error word.  See include/t3.h for the contract.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -32,7 +33,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 
 bool make_u8_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
-                       int box_rows, int box_cols) {
+                       int box_rows, int box_cols, bool swizzle128) {
   std::memset(map, 0, sizeof(*map));
   if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || ld % 16 != 0) return false;
   auto fn = encode_fn();
@@ -42,7 +43,8 @@ bool make_u8_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_t
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) std::memset(map, 0, sizeof(*map));
   return r == CUDA_SUCCESS;
@@ -149,6 +151,46 @@ int run_tc(const uint8_t* a_src, int64_t a_rows, int64_t a_cols, const uint8_t* 
   return launch_tc_dw(p, ma, mb, mo, grid, stream);
 }
 
+// The CTA-pair pipeline for the forward (OP = kOpFwd: act = A [M][K], weights
+// packed along K) or dX (act = dY [M][N], reduction N).  Returns T3_EINVAL
+// without launching when an operand cannot be a TMA source or the output
+// cannot take bulk stores; the caller then uses the single-CTA pipeline.
+template <int OP>
+int run_tc2(const int8_t* act, const uint8_t* Wp, int32_t* out, int64_t M, int64_t N, int64_t K,
+            cudaStream_t stream) {
+  const DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != T3_OK) return st;
+  const int64_t KB = (K + 3) / 4;
+  const int64_t act_cols = (OP == kOpFwd) ? K : N;
+  const int64_t out_cols = (OP == kOpFwd) ? N : K;
+  CUtensorMap ma, mw, mo;
+  if (!make_u8_map_tiled(&ma, act, M, act_cols, act_cols, 128, tc2::BK, true)) return T3_EINVAL;
+  const bool w_ok = (OP == kOpFwd)
+                        ? make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BNH, tc2::BK / 4)
+                        : make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BK, 64);
+  if (!w_ok) return T3_EINVAL;
+  if (!make_i32_map_tiled(&mo, out, M, out_cols, 128, 32, true)) return T3_EINVAL;
+  tc2::Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.out_rows = M;
+  p.out_cols = out_cols;
+  p.num_stages = ceil_div(act_cols, tc2::BK);
+  const int64_t tiles_r = ceil_div(M, tc2::BMP), tiles_c = ceil_div(out_cols, tc2::BN);
+  if (tiles_r * tiles_c > kMaxDim) return T3_EINVAL;
+  p.tiles_r = static_cast<int>(tiles_r);
+  p.tiles_c = static_cast<int>(tiles_c);
+  p.out = out;
+  p.use_tma_out = 1;
+  p.err = dev->err_word;
+  const int64_t pairs = std::min<int64_t>(tiles_r * tiles_c, dev->sms / 2);
+  const int grid = static_cast<int>(2 * pairs);
+  return (OP == kOpFwd) ? launch_tc2_fwd(p, ma, mw, mo, grid, stream)
+                        : launch_tc2_dx(p, ma, mw, mo, grid, stream);
+}
+
 bool bad_dims(int64_t M, int64_t N, int64_t K) {
   return M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim;
 }
@@ -207,6 +249,8 @@ int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64
     if (st != T3_OK) return st;
     return launch_skinny_fwd(A, Wp, C, M, N, K, dev->sms, dev->err_word, stream);
   }
+  const int st2 = run_tc2<kOpFwd>(A, Wp, C, M, N, K, stream);
+  if (st2 != T3_EINVAL) return st2;
   return run_tc<kOpFwd>(reinterpret_cast<const uint8_t*>(A), M, K, Wp, N, KB, C, M, N, K,
                         tc::kChunkKbTernary, stream);
 }
@@ -219,6 +263,8 @@ int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, 
   if (!dY || !Wp || !dX) return T3_EINVAL;
   if (N > kMaxTernaryReduction) return T3_EOVERFLOW;
   const int64_t KB = (K + 3) / 4;
+  const int st2 = run_tc2<kOpDx>(dY, Wp, dX, M, N, K, stream);
+  if (st2 != T3_EINVAL) return st2;
   return run_tc<kOpDx>(reinterpret_cast<const uint8_t*>(dY), M, N, Wp, N, KB, dX, M, K, N,
                        tc::kChunkKbTernary, stream);
 }

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include "t3_tc_gemm.cuh"
+#include "t3_tc2.cuh"
 
 namespace t3 {
 
@@ -19,9 +20,15 @@ int launch_tc_dw(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap& 
 // return false, leaving *map zeroed, when TMA cannot be used (base or row
 // stride not 16-byte aligned, or the driver refuses).
 bool make_u8_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
-                       int box_rows, int box_cols);
+                       int box_rows, int box_cols, bool swizzle128 = false);
 bool make_i32_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
                         int box_rows, int box_cols, bool swizzle128);
+
+// CTA-pair pipeline for the forward and dX products (all operands TMA-able).
+int launch_tc2_fwd(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap& mw,
+                   const CUtensorMap& mo, int grid, cudaStream_t s);
+int launch_tc2_dx(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap& mw,
+                  const CUtensorMap& mo, int grid, cudaStream_t s);
 
 // Small-M forward (M <= 32): zeroes C on `s`, then accumulates into it.
 int launch_skinny_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,

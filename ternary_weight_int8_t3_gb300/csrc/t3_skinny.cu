@@ -33,17 +33,17 @@ namespace sk {
 constexpr int TN = 128;       // weight rows per tile (MMA M, TMEM lanes)
 constexpr int KB = 64;        // reduction elements per unit
 constexpr int GROUP = 16;     // units per activation slice (1024 k)
-constexpr int RAW_STAGES = 16;
+constexpr int RAW_STAGES = 32;
 constexpr int A_STAGES = 4;   // TMEM operand stages, 32 columns each
 constexpr int MP_MAX = 32;
 constexpr int TMEM_COLS = 256;
 constexpr int kAccCol = 0;    // two accumulators of MP_MAX columns
 constexpr int kACol = 64;     // A stages
-constexpr int kDecWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kEpiWarp0 = 6;
-constexpr int kThreads = 320;
+constexpr int kDecWarps = 8;  // two per TMEM lane quadrant, alternating units
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kEpiWarp0 = 10;
+constexpr int kThreads = 448;
 constexpr int kEpiBarrier = 1;
 
 constexpr int RAW_BYTES = TN * (KB / 4);           // 2 KB of packed codes per unit
@@ -127,38 +127,53 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 }
 
 // Activations of k-blocks [kb0, kb1) of group g -> f16 atoms in shared memory,
-// rows m < M (rows up to MP stay zero), in the decode's permuted order.
+// rows m < M (rows up to MP stay zero), in the decode's permuted order.  Each
+// thread loads a batch of 16-byte chunks before converting any, so the L2
+// round trips overlap.
 __device__ __forceinline__ void convert_act(const Params& p, uint8_t* act, int g, int kb0, int kb1,
                                             int tid) {
+  constexpr int kBatch = 8;
   const int chunks_per_row = (kb1 - kb0) * (KB / 16);
   const int total = p.MP * chunks_per_row;
   const bool vec = (p.K % 16 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
-  for (int i = tid; i < total; i += 128) {
-    const int m = i / chunks_per_row, c = i % chunks_per_row;
-    const int kb = kb0 + c / 4, sub = c % 4;  // 16-k chunk `sub` of k-block kb
-    const int64_t k0 = static_cast<int64_t>(kb) * KB + 16 * sub;
-    uint32_t x[4] = {0u, 0u, 0u, 0u};
-    if (m < p.M) {
+  for (int base = 0; base < total; base += 128 * kBatch) {
+    uint4 x[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int i = base + b * 128 + tid;
+      x[b] = make_uint4(0u, 0u, 0u, 0u);
+      if (i >= total) continue;
+      const int m = i / chunks_per_row, c = i % chunks_per_row;
+      const int64_t k0 = static_cast<int64_t>(kb0 + c / 4) * KB + 16 * (c % 4);
+      if (m >= p.M) continue;
       const int8_t* src = p.A + static_cast<int64_t>(m) * p.K + k0;
       if (vec && k0 + 16 <= p.K) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src);
-        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+        x[b] = __ldg(reinterpret_cast<const uint4*>(src));
       } else {
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
         for (int j = 0; j < 16; ++j)
           if (k0 + j < p.K)
-            x[j >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(src[j])) << (8 * (j & 3));
+            w[j >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(__ldg(src + j))) << (8 * (j & 3));
+        x[b] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    uint32_t Y[4];
-    tc::transpose4x4(x[0], x[1], x[2], x[3], Y);  // reduction order 0,4,8,12,1,5,...
-    uint4 o0, o1;
-    tc::s8x4_to_f16(Y[0], o0.x, o0.y);
-    tc::s8x4_to_f16(Y[1], o0.z, o0.w);
-    tc::s8x4_to_f16(Y[2], o1.x, o1.y);
-    tc::s8x4_to_f16(Y[3], o1.z, o1.w);
-    uint8_t* atom = act + (kb - g * GROUP) * ACT_ATOM;
-    *reinterpret_cast<uint4*>(atom + tc::sw128(m, 2 * sub)) = o0;
-    *reinterpret_cast<uint4*>(atom + tc::sw128(m, 2 * sub + 1)) = o1;
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int i = base + b * 128 + tid;
+      if (i >= total) continue;
+      const int m = i / chunks_per_row, c = i % chunks_per_row;
+      const int kb = kb0 + c / 4, sub = c % 4;
+      uint32_t Y[4];
+      tc::transpose4x4(x[b].x, x[b].y, x[b].z, x[b].w, Y);  // reduction order 0,4,8,12,1,5,...
+      uint4 o0, o1;
+      tc::s8x4_to_f16(Y[0], o0.x, o0.y);
+      tc::s8x4_to_f16(Y[1], o0.z, o0.w);
+      tc::s8x4_to_f16(Y[2], o1.x, o1.y);
+      tc::s8x4_to_f16(Y[3], o1.z, o1.w);
+      uint8_t* atom = act + (kb - g * GROUP) * ACT_ATOM;
+      *reinterpret_cast<uint4*>(atom + tc::sw128(m, 2 * sub)) = o0;
+      *reinterpret_cast<uint4*>(atom + tc::sw128(m, 2 * sub + 1)) = o1;
+    }
   }
 }
 
@@ -191,10 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RAW_STAGES; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], kDecWarps);
+      mbar_init(&raw_empty[s], 4);
     }
     for (int s = 0; s < A_STAGES; ++s) {
-      mbar_init(&a_full[s], kDecWarps);
+      mbar_init(&a_full[s], 4);
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -221,10 +236,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kDecWarps) {
     // ------------------------------------------------ weight decode -> TMEM
-    const int q = warp;  // lane quadrant
+    // Warps q and q+4 serve lane quadrant q on alternate units, so that one
+    // decodes while the other waits for its TMEM store to land.
+    const int q = warp & 3, par = warp >> 2;
     const int row = q * 32 + lane;
-    uint32_t rs = 0, rph = 0, as = 0, aph = 0;
-    for (int u = u0; u < u1; ++u) {
+    for (int i = par; u0 + i < u1; i += 2) {
+      const int rs = i % RAW_STAGES, as = i % A_STAGES;
+      const uint32_t rph = (i / RAW_STAGES) & 1, aph = (i / A_STAGES) & 1;
       bool ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2) &&
                 mbar_wait(&a_empty[as], aph ^ 1u, abort_flag, p.err, code_base | 2);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -242,8 +260,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&raw_empty[rs]);
         mbar_arrive(&a_full[as]);
       }
-      if (++rs == RAW_STAGES) { rs = 0; rph ^= 1u; }
-      if (++as == A_STAGES) { as = 0; aph ^= 1u; }
     }
   } else if (warp == kProducerWarp) {
     // --------------------------------------------------- packed weights in

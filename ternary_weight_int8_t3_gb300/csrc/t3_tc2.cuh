@@ -1,0 +1,544 @@
+// t3_tc2.cuh -- CTA-pair tensor-core pipeline for the forward and dX products
+// (sm_103a: tcgen05 cta_group::2, TMEM A operand, TMA, mbarrier).
+//
+// What it computes: the forward product of "t27c PTX backend: ternary x int8
+// GEMM kernel emitted by a .t27 spec (int8 mma.sync), ptx-run glue" ("What
+// this adds": C = A.W, W from 2-bit codes decoded as (c & 1) - ((c >> 1) & 1))
+// and kernel 1 of "spec(igla): hslm_bwd_ptx -- HSLM backward dX and dW as
+// int8 tensor-core PTX written by t27" (dX = dY.W^T with the same codes).
+//
+// Why this shape.  On sm_103a the tensor core has no int8 kind, so both
+// operands travel as exact f16 values.  Expanding them in shared memory costs
+// more shared-memory bandwidth than the tensor core leaves free, so:
+//   * two CTAs on two SMs issue one M=256 MMA (cta_group::2); each CTA holds
+//     128 activation rows and half of the 192 weight rows, halving the weight
+//     operand each SM must write and read;
+//   * the activations are converted in registers and stored into TMEM with
+//     tcgen05.st (the MMA's A operand comes from TMEM), never into shared memory;
+//   * the packed weights are decoded once per tile load into the 128-byte-
+//     swizzled K-major layout the tensor core reads from shared memory;
+//   * stages of 128 reduction elements keep the per-stage control overhead of
+//     the single-thread issue loops below the MMA time.
+// Exactness: the f32 accumulator holds integers of magnitude <= 128 * 65536 =
+// 2^23 per chunk of 65536 reduction elements; chunks are added in int32 by TMA
+// bulk reduce-add.
+//
+// Roles per CTA (704 threads): warps 0-7 convert activations into TMEM, warps
+// 8-15 decode weights into shared memory, warp 16 is the TMA producer, warp
+// 17 issues the MMAs in the even CTA and, in the odd CTA, forwards "stage
+// ready" to the even CTA (one cluster-scope arrive per stage instead of one
+// per converter warp: a cluster-scope release costs the issuing thread
+// hundreds of nanoseconds), warps 18-21 are the epilogue.
+#pragma once
+#include <cstdint>
+#include "t3_tc_gemm.cuh"
+
+namespace t3 {
+namespace tc2 {
+
+constexpr int BMP = 256;        // output rows per pair tile (128 per CTA)
+constexpr int BN = 192;         // output columns per pair tile
+constexpr int BNH = BN / 2;     // weight rows decoded by each CTA
+constexpr int BK = 128;         // reduction elements per stage
+constexpr int RAW_STAGES = 4;
+constexpr int OP_STAGES = 2;
+constexpr int ACC_BUFS = 2;
+constexpr int TMEM_COLS = 512;
+constexpr int kAccCol = 0;                     // 2 x 192 columns
+constexpr int kActCol = ACC_BUFS * BN;         // 2 x 64 columns of f16 pairs
+constexpr int kActWarps = 8;                  // two per TMEM lane quadrant
+constexpr int kWWarps = 8;                    // weight decode
+constexpr int kConvWarps = kActWarps + kWWarps;
+constexpr int kWThreads = 32 * kWWarps;
+constexpr int kProducerWarp = kConvWarps;
+constexpr int kMmaWarp = kConvWarps + 1;      // MMA issuer (even CTA) / forwarder (odd CTA)
+constexpr int kEpiWarp0 = kConvWarps + 2;
+constexpr int kThreads = 32 * (kConvWarps + 2 + 4);
+constexpr int kEpiBarrier = 1;
+constexpr int64_t kChunkStages = 65536 / BK;  // exact f32 chunk for ternary products
+
+constexpr int RAW_A = 128 * BK;                 // [128 rows][128 B], 128-byte swizzle
+template <int OP> struct RawW;
+template <> struct RawW<kOpFwd> { static constexpr int rows = BNH, cols = BK / 4; };  // [96 n][32 B]
+template <> struct RawW<kOpDx> { static constexpr int rows = BK, cols = 64; };         // [128 n][64 B]
+
+template <int OP> struct Layout {
+  static constexpr int raw_w = RawW<OP>::rows * RawW<OP>::cols;
+  static constexpr int raw_stage = ((RAW_A + raw_w) + 1023) / 1024 * 1024;
+  static constexpr int opb_atom = BNH * 128;          // [96 rows][64 f16]
+  static constexpr int opb_stage = 2 * opb_atom;      // two 64-element k atoms
+  static constexpr int stage_out = 128 * 32 * 4;
+  static constexpr int off_opb = 0;
+  static constexpr int off_raw = off_opb + OP_STAGES * opb_stage;
+  static constexpr int off_out = off_raw + RAW_STAGES * raw_stage;
+  static constexpr int off_bar = off_out + 2 * stage_out;
+  static constexpr int n_bars = 2 * RAW_STAGES + 3 * OP_STAGES + 2 * ACC_BUFS + 1;
+  static constexpr int off_misc = off_bar + 8 * n_bars;
+  static constexpr int smem_alloc = off_misc + 16 + 1024;
+};
+
+struct Params {
+  int64_t M, N, K;        // the product's M, N, K
+  int64_t out_rows, out_cols;
+  int64_t num_stages;     // stages along the reduction
+  int tiles_r, tiles_c;
+  int32_t* out;           // used when the output cannot take bulk stores
+  int use_tma_out;
+  int* err;
+};
+
+// ---------------------------------------------------------------- cluster
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// A signal-only arrive on a barrier of the peer CTA.  Used where the data the
+// signal announces never leaves the signalling CTA's SM: the peer half of a
+// pair MMA reads the odd CTA's own shared memory and TMEM, whose writers have
+// already fenced them (proxy fence, tcgen05.wait::st) before handing over.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(dst)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D (both CTAs' TMEM) (+)= A (both CTAs' TMEM) * B (both CTAs' smem halves)^T.
+__device__ __forceinline__ void umma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on `bar` in both CTAs of the pair once all prior MMAs are complete.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_addr(bar)),
+      "h"(static_cast<uint16_t>(0x3))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 16 codes (code i at bits 2i) -> 8 f16x2 words in the permuted reduction
+// order: word 2j = (code j, code j+4), word 2j+1 = (code j+8, code j+12).
+__device__ __forceinline__ void decode16_pairs(uint32_t x, uint32_t* o) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t sh = (j < 3) ? (x << (4 - 2 * j)) : (x >> 2);
+    const uint32_t s = (sh & 0x30303030u) | 0x04040404u;
+    o[2 * j] = prmt(tc::kF16HiTable, 0u, s);
+    o[2 * j + 1] = prmt(tc::kF16HiTable, 0u, s >> 16);
+  }
+}
+
+// ------------------------------------------------------------ converters
+
+// Activation row -> TMEM: thread (quadrant q, half h) owns lane q*32+lane and
+// reduction elements [64h, 64h+64) of the stage, in natural order.  The raw
+// tile is [128][128 B] in the 128-byte swizzle.
+__device__ __forceinline__ void act_to_tmem(const uint8_t* raw_a, uint32_t taddr, int row, int h) {
+  uint32_t v[32];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 x = *reinterpret_cast<const uint4*>(raw_a + tc::sw128(row, 4 * h + c));
+    tc::s8x4_to_f16(x.x, v[8 * c + 0], v[8 * c + 1]);
+    tc::s8x4_to_f16(x.y, v[8 * c + 2], v[8 * c + 3]);
+    tc::s8x4_to_f16(x.z, v[8 * c + 4], v[8 * c + 5]);
+    tc::s8x4_to_f16(x.w, v[8 * c + 6], v[8 * c + 7]);
+  }
+  tmem_st_32x32b_x32(taddr, v);
+}
+
+// Forward weights of this CTA: packed [96 n][32 B] -> f16 [96 n][128 k] as two
+// 64-k atoms, natural order.  Unit = (row, 16-byte half); rows vary fastest so
+// that each 8-thread store phase covers 8 rows.
+__device__ __forceinline__ void decode_w_fwd(const uint8_t* raw_w, uint8_t* opb, int tid) {
+  constexpr int kUnits = BNH * 2;
+  for (int u = tid; u < kUnits; u += kWThreads) {
+    const int row = u % BNH, h = u / BNH;
+    const uint4 x = *reinterpret_cast<const uint4*>(raw_w + row * 32 + 16 * h);
+    uint8_t* atom = opb + h * Layout<kOpFwd>::opb_atom;
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      *reinterpret_cast<uint4*>(atom + tc::sw128(row, 2 * w)) =
+          tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] & 0xFFFFu));
+      *reinterpret_cast<uint4*>(atom + tc::sw128(row, 2 * w + 1)) =
+          tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] >> 16));
+    }
+  }
+}
+
+// dX weights of CTA `rank`: packed [128 n][64 B = 256 k] (the pair uses k-local
+// [0, 192), this CTA [96 rank, 96 rank + 96)) -> f16 [96 k rows][128 n] as two
+// 64-n atoms.  Unit = (word column w of this CTA's 6, n group g of 16, byte
+// half bh): 8 packed words gathered, byte-transposed, decoded per k.  bh is
+// constant across each warp (units are numbered bh-major in blocks of 96).
+__device__ __forceinline__ void decode_w_dx(const uint8_t* raw_w, uint8_t* opb, int tid,
+                                            uint32_t rank) {
+  constexpr int kUnits = 6 * 16 * 2;
+  const uint32_t* rw = reinterpret_cast<const uint32_t*>(raw_w);
+  for (int u = tid; u < kUnits; u += kWThreads) {
+    const int bh = u / 96, g = (u % 96) & 15, wl = (u % 96) >> 4;  // bh warp-uniform, wl < 6
+    const int wcol = 6 * static_cast<int>(rank) + wl;       // word column within the 64-B row
+    uint32_t x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = rw[(8 * g + i) * 16 + wcol];
+    uint32_t Y[4], Z[4];
+    tc::transpose4x4(x[0], x[1], x[2], x[3], Y);
+    tc::transpose4x4(x[4], x[5], x[6], x[7], Z);
+    uint8_t* atom = opb + (g >> 3) * Layout<kOpDx>::opb_atom;
+    const int chunk = g & 7;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      if ((b >> 1) != bh) continue;  // warp-uniform split
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int krow = 16 * wl + 4 * b + j;
+        const uint32_t sy = Y[b] >> (2 * j), sz = Z[b] >> (2 * j);
+        uint4 o;
+        o.x = prmt(tc::kF16HiTable, 0u, ((sy << 4) & 0x3030u) | 0x0404u);
+        o.y = prmt(tc::kF16HiTable, 0u, ((sy >> 12) & 0x3030u) | 0x0404u);
+        o.z = prmt(tc::kF16HiTable, 0u, ((sz << 4) & 0x3030u) | 0x0404u);
+        o.w = prmt(tc::kF16HiTable, 0u, ((sz >> 12) & 0x3030u) | 0x0404u);
+        *reinterpret_cast<uint4*>(atom + tc::sw128(krow, chunk)) = o;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int OP>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tc2_kernel(const Params p, const __grid_constant__ CUtensorMap map_a,
+               const __grid_constant__ CUtensorMap map_w,
+               const __grid_constant__ CUtensorMap map_out) {
+  using L = Layout<OP>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + (((base_addr + 1023u) & ~1023u) - base_addr);
+  uint8_t* opb = smem + L::off_opb;
+  uint8_t* raw = smem + L::off_raw;
+  uint8_t* stage_out = smem + L::off_out;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = raw_full + RAW_STAGES;
+  uint64_t* op_full = raw_empty + RAW_STAGES;   // leader: 16 arrivals (8 warps x 2 CTAs)
+  uint64_t* op_empty = op_full + OP_STAGES;     // both: MMA commit (multicast)
+  uint64_t* acc_full = op_empty + OP_STAGES;    // both: MMA commit (multicast)
+  uint64_t* acc_empty = acc_full + ACC_BUFS;    // leader: 8 arrivals (4 warps x 2 CTAs)
+  uint64_t* op_ready = acc_empty + ACC_BUFS;    // odd CTA: its converters, before forwarding
+  uint64_t* drain_bar = op_ready + OP_STAGES;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::off_misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_misc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int num_tiles = p.tiles_r * p.tiles_c;
+  const int code_base = (OP + 4) << 8;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RAW_STAGES; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], kConvWarps);
+    }
+    for (int s = 0; s < OP_STAGES; ++s) {
+      mbar_init(&op_full[s], kConvWarps + 1);  // own converters + the odd CTA's forwarder
+      mbar_init(&op_empty[s], 1);
+      mbar_init(&op_ready[s], kConvWarps);
+    }
+    for (int s = 0; s < ACC_BUFS; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 8);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp < kConvWarps) {
+    // ---------------------------------------------------------- converters
+    const bool act_warp = warp < kActWarps;
+    const int q = warp & 3, h = (warp >> 2) & 1;
+    const int row = q * 32 + lane;
+    const int wtid = threadIdx.x - kActWarps * 32;
+    uint64_t* signal = (rank == 0) ? op_full : op_ready;  // local, CTA scope
+    uint32_t rs = 0, rph = 0, os = 0, oph = 0;
+    bool ok = true;
+    for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+      for (int64_t kb = 0; kb < p.num_stages; ++kb) {
+        ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2) &&
+             mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const uint8_t* ra = raw + rs * L::raw_stage;
+        if (act_warp) {
+          act_to_tmem(ra, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kActCol +
+                              os * (BK / 2) + 32 * h,
+                      row, h);
+          tmem_wait_st();
+        } else if (OP == kOpFwd) {
+          decode_w_fwd(ra + RAW_A, opb + os * L::opb_stage, wtid);
+          fence_proxy_async_smem();
+        } else {
+          decode_w_dx(ra + RAW_A, opb + os * L::opb_stage, wtid, rank);
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&raw_empty[rs]);
+          mbar_arrive(&signal[os]);
+        }
+        if (++rs == RAW_STAGES) { rs = 0; rph ^= 1u; }
+        if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
+      }
+    }
+  } else if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_a);
+      prefetch_tensormap(&map_w);
+    }
+    uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
+    bool ok = true;
+    for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+      const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
+      const int ay = tr * BMP + static_cast<int>(rank) * 128;
+      int wx, wy;  // weight box origin and its per-stage step
+      if (OP == kOpFwd) {
+        wx = 0;
+        wy = tcol * BN + static_cast<int>(rank) * BNH;
+      } else {
+        wx = tcol * (BN / 4);
+        wy = 0;
+      }
+      for (int64_t kb = 0; kb < p.num_stages; ++kb) {
+        if (lane == 0)
+          ok = mbar_wait(&raw_empty[stage], phase ^ 1u, abort_flag, p.err, code_base | 1);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          uint8_t* dst = raw + stage * L::raw_stage;
+          mbar_arrive_expect_tx(&raw_full[stage], RAW_A + L::raw_w);
+          tma_load_2d(dst, &map_a, &raw_full[stage], static_cast<int>(kb * BK), ay);
+          if (OP == kOpFwd)
+            tma_load_2d(dst + RAW_A, &map_w, &raw_full[stage], static_cast<int>(kb * (BK / 4)), wy);
+          else
+            tma_load_2d(dst + RAW_A, &map_w, &raw_full[stage], wx, static_cast<int>(kb * BK));
+        }
+        issued_mask |= 1u << stage;
+        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == RAW_STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok && lane == 0) {
+      for (int s = 0; s < RAW_STAGES; ++s) {
+        if (!(issued_mask & (1u << s))) continue;
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&raw_full[s], (issued_phase >> s) & 1u) &&
+               global_timer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // --------------------------------------------------- MMA (even CTA)
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(BMP, BN);
+      uint32_t os = 0, oph = 0, ab = 0, aph = 0;
+      bool ok = true, issued_any = false;
+      for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+        for (int64_t c0 = 0; ok && c0 < p.num_stages; c0 += kChunkStages) {
+          const int64_t c1 = (p.num_stages < c0 + kChunkStages) ? p.num_stages : c0 + kChunkStages;
+          ok = mbar_wait(&acc_empty[ab], aph ^ 1u, abort_flag, p.err, code_base | 3);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + kAccCol + ab * BN;
+          for (int64_t kb = c0; kb < c1; ++kb) {
+            ok = mbar_wait(&op_full[os], oph, abort_flag, p.err, code_base | 3);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t b0 = smem_addr(opb + os * L::opb_stage);
+            const uint32_t a0 = tmem_base + kActCol + os * (BK / 2);
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j) {
+              umma_pair_ts(d_tmem, a0 + 8 * j,
+                           smem_desc_k_sw128(b0 + (j >> 2) * L::opb_atom + 32 * (j & 3)), idesc,
+                           (kb > c0 || j > 0) ? 1u : 0u);
+            }
+            issued_any = true;
+            umma_commit_pair(&op_empty[os]);
+            if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
+          }
+          if (!ok) break;
+          umma_commit_pair(&acc_full[ab]);
+          if (++ab == ACC_BUFS) { ab = 0; aph ^= 1u; }
+        }
+      }
+      if (!ok && issued_any) {
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                smem_addr(drain_bar))
+            : "memory");
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    if (rank == 1 && lane == 0) {
+      // forward each stage's readiness to the even CTA's MMA issuer
+      const uint32_t op_full_leader0 = peer_addr(&op_full[0], 0);
+      uint32_t os = 0, oph = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+        for (int64_t kb = 0; kb < p.num_stages; ++kb) {
+          ok = mbar_wait(&op_ready[os], oph, abort_flag, p.err, code_base | 5);
+          if (!ok) break;
+          mbar_arrive_cluster_relaxed(op_full_leader0 + 8u * os);
+          if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int epi_tid = threadIdx.x - kEpiWarp0 * 32;
+    const int srow = q * 32 + lane;
+    const uint32_t acc_empty_leader0 = peer_addr(&acc_empty[0], 0);
+    const bool vec_ok = (p.out_cols % 4 == 0) && (reinterpret_cast<uintptr_t>(p.out) % 16 == 0);
+    uint32_t ab = 0, aph = 0, slab = 0;
+    bool ok = true;
+    if (p.use_tma_out && epi_tid == 0) prefetch_tensormap(&map_out);
+    for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+      const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
+      const int row0 = tr * BMP + static_cast<int>(rank) * 128;
+      const int64_t row = static_cast<int64_t>(row0) + srow;
+      for (int64_t c0 = 0; c0 < p.num_stages; c0 += kChunkStages) {
+        ok = mbar_wait(&acc_full[ab], aph, abort_flag, p.err, code_base | 4);
+        ok = named_bar_and(kEpiBarrier, 128, __all_sync(0xffffffffu, ok));
+        if (!ok) break;
+        tc_fence_after();
+        const bool first = (c0 == 0);
+        if (p.use_tma_out && c0 == kChunkStages && epi_tid == 0) bulk_wait_group<0>();
+        for (int cb = 0; cb < BN / 32; ++cb) {
+          const int64_t col0 = static_cast<int64_t>(tcol) * BN + cb * 32;
+          if (col0 >= p.out_cols) break;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + ab * BN +
+                                 cb * 32,
+                             v);
+          tmem_wait_ld();
+          if (p.use_tma_out) {
+            uint8_t* buf = stage_out + (slab & 1) * L::stage_out;
+            if (epi_tid == 0) bulk_wait_group_read<1>();
+            named_bar_sync(kEpiBarrier, 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int4 val =
+                  make_int4(tc::f32_bits_to_i32(v[4 * c]), tc::f32_bits_to_i32(v[4 * c + 1]),
+                            tc::f32_bits_to_i32(v[4 * c + 2]), tc::f32_bits_to_i32(v[4 * c + 3]));
+              *reinterpret_cast<int4*>(buf + tc::sw128(srow, c)) = val;
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(kEpiBarrier, 128);
+            if (epi_tid == 0) {
+              if (first)
+                tma_store_2d(&map_out, buf, static_cast<int>(col0), row0);
+              else
+                tma_reduce_add_2d(&map_out, buf, static_cast<int>(col0), row0);
+              bulk_commit_group();
+            }
+            ++slab;
+          } else if (row < p.out_rows) {
+            const int64_t rem = p.out_cols - col0;
+            tc::store_row32(p.out + row * p.out_cols + col0, v, rem < 32 ? static_cast<int>(rem) : 32,
+                            first, vec_ok);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * ab);
+        if (++ab == ACC_BUFS) { ab = 0; aph ^= 1u; }
+      }
+    }
+    if (p.use_tma_out && epi_tid == 0) bulk_wait_group<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's TMEM and barriers stay alive until both CTAs are done
+  tc_fence_after();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace tc2
+}  // namespace t3

@@ -22,4 +22,21 @@ int launch_tc_fwd(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap&
   return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
 }
 
+int launch_tc2_fwd(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap& mw,
+                   const CUtensorMap& mo, int grid, cudaStream_t s) {
+  constexpr int kSmem = tc2::Layout<kOpFwd>::smem_alloc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
+  static std::atomic<bool> attr_done[64];
+  if (dev < 0 || dev >= 64) return T3_EDEVICE;
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(tc2::tc2_kernel<kOpFwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmem) != cudaSuccess)
+      return T3_ECUDA;
+    attr_done[dev].store(true, std::memory_order_release);
+  }
+  tc2::tc2_kernel<kOpFwd><<<grid, tc2::kThreads, kSmem, s>>>(p, ma, mw, mo);
+  return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
+}
+
 }  // namespace t3
