@@ -143,7 +143,9 @@ SMALL_M = [(m, n, k) for (n, k) in ((3456, 1280), (8192, 8192)) for m in (1, 8, 
 def bench_small_m(t3, torch, dev, stream, hbm_gbs, reps=30):
     """Small-M forward sweep: bytes moved (packed weights + activations + the
     int32 output) per call over its device time.  Enough distinct copies of Wp
-    rotate through the calls that no copy is still in the 129 MB L2."""
+    rotate through the calls that no copy is still in the 129 MB L2.  The calls
+    are captured once in a CUDA graph and replayed, so the device time is not
+    hidden behind host launch overhead (a call is a memset of C plus one kernel)."""
     out = []
     for (m, n, k) in SMALL_M:
         wl = t3_synth.BY_NAME[f"skinny_m{m}_n{n}_k{k}"]
@@ -157,10 +159,23 @@ def bench_small_m(t3, torch, dev, stream, hbm_gbs, reps=30):
         for i in range(3):
             t3.t3_gemm_fwd(A_d, wps[i % copies], K=k, C=C, stream=stream)
         torch.cuda.synchronize(dev)
+        mode = "graph"
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(reps):
+                    t3.t3_gemm_fwd(A_d, wps[i % copies], K=k, C=C)
+            run = g.replay
+        except Exception:  # capture unsupported here: time the eager calls
+            mode = "eager"
+            def run():
+                for i in range(reps):
+                    t3.t3_gemm_fwd(A_d, wps[i % copies], K=k, C=C, stream=stream)
+        run()
+        torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(reps):
-            t3.t3_gemm_fwd(A_d, wps[i % copies], K=k, C=C, stream=stream)
+        run()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         us = e0.elapsed_time(e1) * 1e3 / reps
@@ -168,7 +183,7 @@ def bench_small_m(t3, torch, dev, stream, hbm_gbs, reps=30):
         gbs = nbytes / (us * 1e-6) / 1e9
         out.append({"M": m, "N": n, "K": k, "us_per_call": round(us, 3), "bytes": nbytes,
                     "GBps": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 3),
-                    "TOPS": round(2 * m * n * k / (us * 1e-6) / 1e12, 2)})
+                    "TOPS": round(2 * m * n * k / (us * 1e-6) / 1e12, 2), "timing": mode})
         del wps
     return out
 

@@ -1,27 +1,28 @@
-// t3_skinny.cu -- the small-M forward (M <= 32): C = A . W read at the rate
-// of the packed weights.
+// t3_skinny.cu -- the small-M forward (M <= 32): C = A . W at the rate of
+// reading the packed weights.
 //
 // What it computes: the forward product of "t27c PTX backend: ternary x int8
 // GEMM kernel emitted by a .t27 spec (int8 mma.sync), ptx-run glue", section
 // "What this adds": C[m][n] = sum_k A[m][k] W[k][n], W from 2-bit codes.
 //
-// With M <= 32 the work per packed weight byte is tiny and the product is
+// With M <= 32 there is little work per packed weight byte and the product is
 // bound by streaming Wp (N * ceil(K/4) bytes) from HBM once.  The pages have no
 // such path; this one is built for sm_103a:
 //   * swap-AB on the tensor core: D[n][m] = W^T[n][k] . A^T[k][m] with
-//     tcgen05.mma kind::f16, M=128 weight rows, N = 16 or 32 activation rows.
+//     tcgen05.mma kind::f16, M = 128 weight rows, N = 16 or 32 activation rows;
 //   * the weights are decoded in registers straight into TMEM (the MMA's A
-//     operand comes from TMEM), so the 8x-expanded f16 weights never touch
-//     shared memory;
+//     operand comes from TMEM), so the 8x-expanded weights never touch shared
+//     memory; each unit is 128 weight rows x 384 k (a 12 KB TMA box), so that
+//     every SM goes through only a handful of synchronisation rounds;
 //   * the decode pairs code j with code j+4 of each 16-code word (two byte
 //     permutes per four weights); the activations are written in the same
 //     permuted reduction order, so every product and sum is unchanged;
-//   * the (k-group, weight tile, k-block) units are split evenly over all
-//     SMs; each run of units that shares a weight tile ends with a TMA
-//     reduce-add of its int32 partial tile into C, which the host zeroes
-//     first.  Integer addition makes the result independent of the order.
-//   * a run never spans more than 16 k-blocks (1024 k), so its f32 sum is an
-//     integer of magnitude <= 2^17 and converts to int32 exactly.
+//   * the units, ordered (k-group, weight tile, k-unit), are split evenly over
+//     the SMs; each run of units that shares a weight tile ends with a TMA
+//     reduce-add of its int32 partial into C, which the host zeroes first.
+//     Integer addition makes the result independent of the order.
+//   * a run spans at most one k-group (1536 k), so its f32 sum is an integer of
+//     magnitude <= 128 * 1536 < 2^18 and converts to int32 exactly.
 #include <atomic>
 
 #include "t3.h"
@@ -30,30 +31,33 @@
 namespace t3 {
 namespace sk {
 
-constexpr int TN = 128;       // weight rows per tile (MMA M, TMEM lanes)
-constexpr int KB = 64;        // reduction elements per unit
-constexpr int GROUP = 16;     // units per activation slice (1024 k)
-constexpr int RAW_STAGES = 32;
-constexpr int A_STAGES = 4;   // TMEM operand stages, 32 columns each
+constexpr int TN = 128;          // weight rows per tile (MMA M, TMEM lanes)
+constexpr int UK = 384;          // reduction elements per unit
+constexpr int UB = UK / 4;       // packed bytes per row per unit (96)
+constexpr int GROUP = 4;         // units per activation slice (1536 k)
+constexpr int GK = GROUP * UK;
+constexpr int RAW_STAGES = 4;
+constexpr int A_BUFS = 2;        // TMEM operand buffers of UK/2 columns
 constexpr int MP_MAX = 32;
-constexpr int TMEM_COLS = 256;
-constexpr int kAccCol = 0;    // two accumulators of MP_MAX columns
-constexpr int kACol = 64;     // A stages
-constexpr int kDecWarps = 8;  // two per TMEM lane quadrant, alternating units
+constexpr int TMEM_COLS = 512;
+constexpr int kAccCol = 0;       // two accumulators of MP_MAX columns
+constexpr int kACol = 64;        // two unit buffers of 192 columns
+constexpr int kDecWarps = 8;     // two per lane quadrant: halves of the unit
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kEpiWarp0 = 10;
 constexpr int kThreads = 448;
 constexpr int kEpiBarrier = 1;
 
-constexpr int RAW_BYTES = TN * (KB / 4);           // 2 KB of packed codes per unit
-constexpr int ACT_ATOM = MP_MAX * 128;             // [32 rows][64 f16] per k-block
+constexpr int RAW_BYTES = TN * UB;                 // 12 KB of codes per unit
+constexpr int ACT_ATOM = MP_MAX * 128;             // [32 rows][64 f16] per 64 k
+constexpr int ACT_ATOMS = GK / 64;                 // 24 atoms = 96 KB
 constexpr int STAGE_OUT = MP_MAX * TN * 4;         // [32 rows][128 int32]
 constexpr int OFF_ACT = 0;
-constexpr int OFF_RAW = OFF_ACT + GROUP * ACT_ATOM;
+constexpr int OFF_RAW = OFF_ACT + ACT_ATOMS * ACT_ATOM;
 constexpr int OFF_OUT = OFF_RAW + RAW_STAGES * RAW_BYTES;
 constexpr int OFF_BAR = OFF_OUT + 2 * STAGE_OUT;
-constexpr int N_BARS = 2 * RAW_STAGES + 2 * A_STAGES + 4 + 2;
+constexpr int N_BARS = 2 * RAW_STAGES + 2 * A_BUFS + 4 + 2;
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
 constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
 
@@ -62,29 +66,40 @@ struct Params {
   const uint8_t* Wp;   // [N][ceil(K/4)]
   int32_t* C;          // [M][N], zeroed by the host
   int M, N, K, MP;
-  int kb_total, tiles, units, units_per_group_row;
+  int units_total, tiles, units_k;  // units along k per tile
   int use_tma_w, use_tma_out;
   int* err;
 };
 
-struct Unit {
-  int g, t, kb;  // activation group, weight tile, global k-block
+// Walks units in (k-group, tile, k-unit) order; only the starting unit is
+// decoded with divisions.
+struct UnitIter {
+  int g, t, uk;       // k-group, tile, unit within the group
+  int nk;             // units in the current group
+  int tiles, units_k;
+  __device__ void init(const Params& p, int u) {
+    tiles = p.tiles;
+    units_k = p.units_k;
+    const int full = tiles * GROUP;
+    g = u / full;
+    nk = min(GROUP, units_k - g * GROUP);
+    const int rem = u - g * full;
+    t = rem / nk;
+    uk = rem % nk;
+  }
+  __device__ int k_unit() const { return g * GROUP + uk; }
+  __device__ void next() {
+    if (++uk == nk) {
+      uk = 0;
+      if (++t == tiles) {
+        t = 0;
+        ++g;
+        nk = min(GROUP, units_k - g * GROUP);
+      }
+    }
+  }
+  __device__ bool last_of_run() const { return uk + 1 == nk; }
 };
-
-__device__ __forceinline__ Unit unit_at(const Params& p, int u) {
-  const int full = p.tiles * GROUP;  // units in a full group
-  Unit r;
-  r.g = u / full;
-  const int rem = u - r.g * full;
-  const int nk = min(GROUP, p.kb_total - r.g * GROUP);
-  r.t = rem / nk;
-  r.kb = r.g * GROUP + rem % nk;
-  return r;
-}
-
-__device__ __forceinline__ bool same_run(const Unit& a, const Unit& b) {
-  return a.g == b.g && a.t == b.t;
-}
 
 // 16 codes (one word, code i at bits 2i) -> 8 f16x2 words in the permuted
 // reduction order: word 2j = (code j, code j+4), word 2j+1 = (code j+8, code j+12).
@@ -98,24 +113,6 @@ __device__ __forceinline__ void decode16_pairs(uint32_t x, uint32_t* o) {
   }
 }
 
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
-      "%29, %30, %31, %32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-      "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc]^T, f16 operands, f32 accumulate.
 __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -126,14 +123,14 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-// Activations of k-blocks [kb0, kb1) of group g -> f16 atoms in shared memory,
+// Activations of units [uk0, uk1) of k-group g -> f16 atoms in shared memory,
 // rows m < M (rows up to MP stay zero), in the decode's permuted order.  Each
-// thread loads a batch of 16-byte chunks before converting any, so the L2
-// round trips overlap.
-__device__ __forceinline__ void convert_act(const Params& p, uint8_t* act, int g, int kb0, int kb1,
+// thread loads a batch of 16-byte chunks before converting any.
+__device__ __forceinline__ void convert_act(const Params& p, uint8_t* act, int g, int uk0, int uk1,
                                             int tid) {
   constexpr int kBatch = 8;
-  const int chunks_per_row = (kb1 - kb0) * (KB / 16);
+  const int k_base = g * GK + uk0 * UK;
+  const int chunks_per_row = (uk1 - uk0) * (UK / 16);
   const int total = p.MP * chunks_per_row;
   const bool vec = (p.K % 16 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
   for (int base = 0; base < total; base += 128 * kBatch) {
@@ -144,7 +141,7 @@ __device__ __forceinline__ void convert_act(const Params& p, uint8_t* act, int g
       x[b] = make_uint4(0u, 0u, 0u, 0u);
       if (i >= total) continue;
       const int m = i / chunks_per_row, c = i % chunks_per_row;
-      const int64_t k0 = static_cast<int64_t>(kb0 + c / 4) * KB + 16 * (c % 4);
+      const int64_t k0 = static_cast<int64_t>(k_base) + 16 * c;
       if (m >= p.M) continue;
       const int8_t* src = p.A + static_cast<int64_t>(m) * p.K + k0;
       if (vec && k0 + 16 <= p.K) {
@@ -162,7 +159,7 @@ __device__ __forceinline__ void convert_act(const Params& p, uint8_t* act, int g
       const int i = base + b * 128 + tid;
       if (i >= total) continue;
       const int m = i / chunks_per_row, c = i % chunks_per_row;
-      const int kb = kb0 + c / 4, sub = c % 4;
+      const int kk = uk0 * UK + 16 * c;  // offset within the group
       uint32_t Y[4];
       tc::transpose4x4(x[b].x, x[b].y, x[b].z, x[b].w, Y);  // reduction order 0,4,8,12,1,5,...
       uint4 o0, o1;
@@ -170,7 +167,8 @@ __device__ __forceinline__ void convert_act(const Params& p, uint8_t* act, int g
       tc::s8x4_to_f16(Y[1], o0.z, o0.w);
       tc::s8x4_to_f16(Y[2], o1.x, o1.y);
       tc::s8x4_to_f16(Y[3], o1.z, o1.w);
-      uint8_t* atom = act + (kb - g * GROUP) * ACT_ATOM;
+      uint8_t* atom = act + (kk >> 6) * ACT_ATOM;
+      const int sub = (kk & 63) >> 4;
       *reinterpret_cast<uint4*>(atom + tc::sw128(m, 2 * sub)) = o0;
       *reinterpret_cast<uint4*>(atom + tc::sw128(m, 2 * sub + 1)) = o1;
     }
@@ -190,8 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + RAW_STAGES;
   uint64_t* a_full = raw_empty + RAW_STAGES;
-  uint64_t* a_empty = a_full + A_STAGES;
-  uint64_t* acc_full = a_empty + A_STAGES;
+  uint64_t* a_empty = a_full + A_BUFS;
+  uint64_t* acc_full = a_empty + A_BUFS;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* act_full = acc_empty + 2;
   uint64_t* drain_bar = act_full + 1;
@@ -199,17 +197,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int u0 = static_cast<int>(static_cast<int64_t>(p.units) * blockIdx.x / gridDim.x);
-  const int u1 = static_cast<int>(static_cast<int64_t>(p.units) * (blockIdx.x + 1) / gridDim.x);
+  const int u0 = static_cast<int>(static_cast<int64_t>(p.units_total) * blockIdx.x / gridDim.x);
+  const int u1 =
+      static_cast<int>(static_cast<int64_t>(p.units_total) * (blockIdx.x + 1) / gridDim.x);
+  const int n_units = u1 - u0;
   constexpr int code_base = 4 << 8;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < RAW_STAGES; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 4);
+      mbar_init(&raw_empty[s], kDecWarps);
     }
-    for (int s = 0; s < A_STAGES; ++s) {
-      mbar_init(&a_full[s], 4);
+    for (int s = 0; s < A_BUFS; ++s) {
+      mbar_init(&a_full[s], kDecWarps);
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -221,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  // activation atoms: rows MP..31 are never written, keep them zero
-  for (int i = threadIdx.x; i < GROUP * ACT_ATOM / 16; i += kThreads)
+  // rows MP..31 of the activation atoms are never written: keep them zero
+  for (int i = threadIdx.x; i < ACT_ATOMS * ACT_ATOM / 16; i += kThreads)
     reinterpret_cast<uint4*>(act)[i] = make_uint4(0, 0, 0, 0);
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_holder, TMEM_COLS);
@@ -236,29 +236,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kDecWarps) {
     // ------------------------------------------------ weight decode -> TMEM
-    // Warps q and q+4 serve lane quadrant q on alternate units, so that one
-    // decodes while the other waits for its TMEM store to land.
-    const int q = warp & 3, par = warp >> 2;
+    const int q = warp & 3, h = warp >> 2;  // lane quadrant, half of the unit
     const int row = q * 32 + lane;
-    for (int i = par; u0 + i < u1; i += 2) {
-      const int rs = i % RAW_STAGES, as = i % A_STAGES;
-      const uint32_t rph = (i / RAW_STAGES) & 1, aph = (i / A_STAGES) & 1;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    for (int i = 0; i < n_units; ++i) {
+      const int rs = i & (RAW_STAGES - 1), ab = i & (A_BUFS - 1);
+      const uint32_t rph = (i / RAW_STAGES) & 1, aph = (i / A_BUFS) & 1;
       bool ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2) &&
-                mbar_wait(&a_empty[as], aph ^ 1u, abort_flag, p.err, code_base | 2);
+                mbar_wait(&a_empty[ab], aph ^ 1u, abort_flag, p.err, code_base | 2);
       if (!__all_sync(0xffffffffu, ok)) break;
-      const uint4 x = *reinterpret_cast<const uint4*>(raw + rs * RAW_BYTES + row * 16);
-      uint32_t v[32];
-      decode16_pairs(x.x, v);
-      decode16_pairs(x.y, v + 8);
-      decode16_pairs(x.z, v + 16);
-      decode16_pairs(x.w, v + 24);
-      tmem_st_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kACol + as * 32, v);
-      tmem_wait_st();
+      // 48 bytes = 12 words = 192 codes of this row's half of the unit
+      const uint8_t* src = raw + rs * RAW_BYTES + row * UB + 48 * h;
+      const uint32_t col0 = kACol + ab * (UK / 2) + 96 * h;
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {
+        const uint4 x = *reinterpret_cast<const uint4*>(src + 16 * part);
+        uint32_t v[32];
+        decode16_pairs(x.x, v);
+        decode16_pairs(x.y, v + 8);
+        decode16_pairs(x.z, v + 16);
+        decode16_pairs(x.w, v + 24);
+        tc2::tmem_st_32x32b_x32(lane_addr + col0 + 32 * part, v);
+      }
+      tc2::tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&raw_empty[rs]);
-        mbar_arrive(&a_full[as]);
+        mbar_arrive(&a_full[ab]);
       }
     }
   } else if (warp == kProducerWarp) {
@@ -267,20 +272,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
     bool ok = true;
     const int64_t kbytes = (static_cast<int64_t>(p.K) + 3) / 4;
-    for (int u = u0; u < u1; ++u) {
-      ok = mbar_wait(&raw_empty[stage], phase ^ 1u, abort_flag, p.err, code_base | 1);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      const Unit un = unit_at(p, u);
+    UnitIter it;
+    it.init(p, u0);
+    for (int i = 0; i < n_units; ++i, it.next()) {
+      if (lane == 0)
+        ok = mbar_wait(&raw_empty[stage], phase ^ 1u, abort_flag, p.err, code_base | 1);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
       uint8_t* dst = raw + stage * RAW_BYTES;
-      if (!p.use_tma_w)
-        tc::manual_box(dst, p.Wp, kbytes, p.N, kbytes, static_cast<int64_t>(un.t) * TN,
-                       static_cast<int64_t>(un.kb) * (KB / 4), TN, KB / 4, lane);
-      __threadfence_block();
-      __syncwarp();
+      const int x0 = it.k_unit() * UB, y0 = it.t * TN;
+      if (!p.use_tma_w) {
+        tc::manual_box(dst, p.Wp, kbytes, p.N, kbytes, y0, x0, TN, UB, lane);
+        __threadfence_block();
+        __syncwarp();
+      }
       if (lane == 0) {
         if (p.use_tma_w) {
           mbar_arrive_expect_tx(&raw_full[stage], RAW_BYTES);
-          tma_load_2d(dst, &map_w, &raw_full[stage], un.kb * (KB / 4), un.t * TN);
+          tma_load_2d(dst, &map_w, &raw_full[stage], x0, y0);
         } else {
           mbar_arrive(&raw_full[stage]);
         }
@@ -302,43 +311,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16_f32(TN, p.MP);
-      uint32_t as = 0, aph = 0, ab = 0, abph = 0, actph = 0;
+      uint32_t acc_b = 0, acc_ph = 0, act_ph = 0;
       int cur_g = -1;
-      bool ok = true, issued_any = false;
-      Unit prev{-1, -1, -1};
-      for (int u = u0; ok && u < u1; ++u) {
-        const Unit un = unit_at(p, u);
-        const bool seg_first = !same_run(un, prev);
-        const bool seg_last = (u + 1 == u1) || !same_run(un, unit_at(p, u + 1));
+      bool ok = true, issued_any = false, seg_first = true;
+      UnitIter it;
+      it.init(p, u0);
+      for (int i = 0; i < n_units; ++i, it.next()) {
+        const int ab = i & (A_BUFS - 1);
+        const uint32_t aph = (i / A_BUFS) & 1;
+        const bool seg_last = (i + 1 == n_units) || it.last_of_run();
         if (seg_first) {
-          ok = mbar_wait(&acc_empty[ab], abph ^ 1u, abort_flag, p.err, code_base | 3);
-          if (ok && un.g != cur_g) {
-            ok = mbar_wait(act_full, actph, abort_flag, p.err, code_base | 3);
-            actph ^= 1u;
-            cur_g = un.g;
+          ok = mbar_wait(&acc_empty[acc_b], acc_ph ^ 1u, abort_flag, p.err, code_base | 3);
+          if (ok && it.g != cur_g) {
+            ok = mbar_wait(act_full, act_ph, abort_flag, p.err, code_base | 3);
+            act_ph ^= 1u;
+            cur_g = it.g;
           }
         }
-        if (ok) ok = mbar_wait(&a_full[as], aph, abort_flag, p.err, code_base | 3);
+        if (ok) ok = mbar_wait(&a_full[ab], aph, abort_flag, p.err, code_base | 3);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t b0 = smem_addr(act + (un.kb - un.g * GROUP) * ACT_ATOM);
-        const uint32_t d_tmem = tmem_base + kAccCol + ab * MP_MAX;
-        const uint32_t a_tmem = tmem_base + kACol + as * 32;
-#pragma unroll
-        for (int j = 0; j < KB / 16; ++j)
-          umma_f16_ts(d_tmem, a_tmem + 8 * j, smem_desc_k_sw128(b0 + 32 * j), idesc,
+        const uint32_t b0 = smem_addr(act + it.uk * (UK / 64) * ACT_ATOM);
+        const uint32_t d_tmem = tmem_base + kAccCol + acc_b * MP_MAX;
+        const uint32_t a_tmem = tmem_base + kACol + ab * (UK / 2);
+#pragma unroll 4
+        for (int j = 0; j < UK / 16; ++j)
+          umma_f16_ts(d_tmem, a_tmem + 8 * j,
+                      smem_desc_k_sw128(b0 + (j >> 2) * ACT_ATOM + 32 * (j & 3)), idesc,
                       (!seg_first || j > 0) ? 1u : 0u);
         issued_any = true;
-        umma_commit(&a_empty[as]);
-        if (++as == A_STAGES) { as = 0; aph ^= 1u; }
+        umma_commit(&a_empty[ab]);
+        seg_first = seg_last;
         if (seg_last) {
-          umma_commit(&acc_full[ab]);
-          if (++ab == 2) { ab = 0; abph ^= 1u; }
+          umma_commit(&acc_full[acc_b]);
+          if (++acc_b == 2) { acc_b = 0; acc_ph ^= 1u; }
         }
-        prev = un;
       }
       if (!ok && issued_any) {
-        // Let the tensor core finish what was issued before TMEM is released.
         umma_commit(drain_bar);
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
@@ -351,42 +360,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int etid = threadIdx.x - kEpiWarp0 * 32;
     const int nloc = q * 32 + lane;
-    uint32_t ab = 0, abph = 0, slab = 0;
+    uint32_t acc_b = 0, acc_ph = 0, slab = 0;
     int cur_g = -1;
     if (p.use_tma_out && etid == 0) prefetch_tensormap(&map_out);
-    int u = u0;
-    while (u < u1) {
-      const Unit first = unit_at(p, u);
-      int v = u + 1;
-      while (v < u1 && same_run(first, unit_at(p, v))) ++v;
-      if (first.g != cur_g) {
-        // k-blocks of this group that this CTA's remaining units touch
-        int kb_lo = first.kb, kb_hi = first.kb + 1;
-        for (int w = u; w < u1; ++w) {
-          const Unit x = unit_at(p, w);
-          if (x.g != first.g) break;
-          kb_lo = min(kb_lo, x.kb);
-          kb_hi = max(kb_hi, x.kb + 1);
+    UnitIter it;
+    it.init(p, u0);
+    int i = 0;
+    while (i < n_units) {
+      // the run of units that shares (k-group, tile) with unit i
+      const int g = it.g, t = it.t, uk_first = it.uk;
+      int len = 1;
+      while (i + len < n_units && !it.last_of_run()) {
+        it.next();
+        ++len;
+      }
+      const int uk_last = it.uk;
+      if (g != cur_g) {
+        // k-units of this group that this CTA's remaining runs touch
+        int lo = uk_first, hi = uk_last + 1;
+        UnitIter scan = it;
+        for (int j = i + len; j < n_units; ++j) {
+          scan.next();
+          if (scan.g != g) break;
+          lo = min(lo, scan.uk);
+          hi = max(hi, scan.uk + 1);
         }
-        convert_act(p, act, first.g, kb_lo, kb_hi, etid);
+        convert_act(p, act, g, lo, hi, etid);
         fence_proxy_async_smem();
         named_bar_sync(kEpiBarrier, 128);
         if (etid == 0) mbar_arrive(act_full);
-        cur_g = first.g;
+        cur_g = g;
       }
-      bool ok = mbar_wait(&acc_full[ab], abph, abort_flag, p.err, code_base | 4);
+      bool ok = mbar_wait(&acc_full[acc_b], acc_ph, abort_flag, p.err, code_base | 4);
       ok = named_bar_and(kEpiBarrier, 128, __all_sync(0xffffffffu, ok));
       if (!ok) break;
       tc_fence_after();
       uint32_t val[32];
-      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + ab * MP_MAX,
-                         val);
+      tmem_ld_32x32b_x32(
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + acc_b * MP_MAX, val);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[ab]);
-      if (++ab == 2) { ab = 0; abph ^= 1u; }
-      const int64_t n = static_cast<int64_t>(first.t) * TN + nloc;
+      if (lane == 0) mbar_arrive(&acc_empty[acc_b]);
+      if (++acc_b == 2) { acc_b = 0; acc_ph ^= 1u; }
+      const int64_t n = static_cast<int64_t>(t) * TN + nloc;
       if (p.use_tma_out) {
         uint8_t* buf = stage_out + (slab & 1) * STAGE_OUT;
         if (etid == 0) bulk_wait_group_read<1>();
@@ -398,16 +415,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         named_bar_sync(kEpiBarrier, 128);
         if (etid == 0) {
-          tma_reduce_add_2d(&map_out, buf, first.t * TN, 0);
+          tma_reduce_add_2d(&map_out, buf, t * TN, 0);
           bulk_commit_group();
         }
         ++slab;
       } else if (n < p.N) {
 #pragma unroll
         for (int m = 0; m < MP_MAX; ++m)
-          if (m < p.M) atomicAdd(p.C + static_cast<int64_t>(m) * p.N + n, tc::f32_bits_to_i32(val[m]));
+          if (m < p.M)
+            atomicAdd(p.C + static_cast<int64_t>(m) * p.N + n, tc::f32_bits_to_i32(val[m]));
       }
-      u = v;
+      i += len;
+      if (i < n_units) it.next();
     }
     if (p.use_tma_out && etid == 0) bulk_wait_group<0>();
   }
@@ -433,20 +452,19 @@ int launch_skinny_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M,
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.MP = M <= 16 ? 16 : 32;
-  p.kb_total = static_cast<int>((K + sk::KB - 1) / sk::KB);
+  p.units_k = static_cast<int>((K + sk::UK - 1) / sk::UK);
   p.tiles = static_cast<int>((N + sk::TN - 1) / sk::TN);
-  const int64_t units = static_cast<int64_t>(p.kb_total) * p.tiles;
+  const int64_t units = static_cast<int64_t>(p.units_k) * p.tiles;
   if (units > 2147483647LL) return T3_EINVAL;
-  p.units = static_cast<int>(units);
+  p.units_total = static_cast<int>(units);
   p.err = err;
   const int64_t kbytes = (K + 3) / 4;
   CUtensorMap mw, mo;
-  p.use_tma_w = make_u8_map_tiled(&mw, Wp, N, kbytes, kbytes, sk::TN, sk::KB / 4) ? 1 : 0;
+  p.use_tma_w = make_u8_map_tiled(&mw, Wp, N, kbytes, kbytes, sk::TN, sk::UB) ? 1 : 0;
   p.use_tma_out = make_i32_map_tiled(&mo, C, M, N, p.MP, sk::TN, false) ? 1 : 0;
   if (cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * sizeof(int32_t), s) != cudaSuccess)
     return T3_ECUDA;
-  int grid = static_cast<int>((units + 3) / 4);
-  if (grid > sms) grid = sms;
+  int grid = static_cast<int>(units < sms ? units : sms);
   if (grid < 1) grid = 1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
