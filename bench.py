@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-small-m", action="store_true",
+                    help="skip the small-M forward sweep (for launch-list captures)")
     return ap.parse_args()
 
 
@@ -138,6 +140,42 @@ class ClockSampler:
 
 
 SMALL_M = [(m, n, k) for (n, k) in ((3456, 1280), (8192, 8192)) for m in (1, 8, 27)]
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_layer_step_16384x3456x1280.md")
+
+
+def csrc_digest():
+    """sha256 over the CUDA sources, in name order: a captured traffic figure
+    only describes the kernels it was taken from."""
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "ternary_weight_int8_t3_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def dram_traffic(product):
+    """DRAM bytes (read + write) per launch of `product` from the committed ncu
+    summary, or None when it is absent or the kernels changed since."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    digest, per = None, {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            line = line.strip().strip("`")
+            if line.startswith("csrc_sha256:"):
+                digest = line.split(":", 1)[1].strip()
+            elif line.startswith("dram_bytes_per_launch:"):
+                for item in line.split(":", 1)[1].split(","):
+                    k, v = item.strip().split("=")
+                    per[k] = int(v)
+    if digest != csrc_digest():
+        return None
+    return per.get(product)
 
 
 def bench_small_m(t3, torch, dev, stream, hbm_gbs, reps=30):
@@ -384,11 +422,7 @@ def main():
         peak_note = ("sustained" if long_region else "burst") + " bf16 dense of measured; f16 runs at the bf16 rate"
     else:
         peak, peak_note = FALLBACK_TFLOPS, "bf16 dense of fallback; f16 runs at the bf16 rate"
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
-            traffic = json.load(f).get(dominant)
+    traffic = dram_traffic(dominant)
     kname = {"fwd": "t3_gemm_fwd", "dx": "t3_gemm_bwd_dx", "dw": "t3_gemm_bwd_dw"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -410,7 +444,8 @@ def main():
         "clocks": clocks.summary(),
     }
     hbm = peaks.get("hbm_gbs", 6800.0) if peak_src == "measured" else 6800.0
-    line["small_m"] = {"hbm_peak_GBps": hbm, "calls": bench_small_m(t3, torch, dev, stream, hbm)}
+    if not args.no_small_m:
+        line["small_m"] = {"hbm_peak_GBps": hbm, "calls": bench_small_m(t3, torch, dev, stream, hbm)}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(A, w, dY)
     print(json.dumps(line), flush=True)

@@ -191,6 +191,31 @@ int run_tc2(const int8_t* act, const uint8_t* Wp, int32_t* out, int64_t M, int64
                         : launch_tc2_dx(p, ma, mw, mo, grid, stream);
 }
 
+// The CTA-pair dW pipeline.  Returns T3_EINVAL without launching when A, dY or
+// dW cannot be used with TMA; the caller then uses the single-CTA pipeline.
+int run_dw2(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N, int64_t K,
+            cudaStream_t stream) {
+  const DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != T3_OK) return st;
+  CUtensorMap ma, mdy, mo;
+  if (!make_u8_map_tiled(&ma, A, M, K, K, dw2::BK, 128)) return T3_EINVAL;
+  if (!make_u8_map_tiled(&mdy, dY, M, N, N, dw2::BK, 128)) return T3_EINVAL;
+  if (!make_i32_map_tiled(&mo, dW, K, N, 128, 32, true)) return T3_EINVAL;
+  dw2::Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.num_stages = ceil_div(M, dw2::BK);
+  const int64_t tiles_r = ceil_div(K, dw2::BMP), tiles_c = ceil_div(N, dw2::BN);
+  if (tiles_r * tiles_c > kMaxDim) return T3_EINVAL;
+  p.tiles_r = static_cast<int>(tiles_r);
+  p.tiles_c = static_cast<int>(tiles_c);
+  p.err = dev->err_word;
+  const int64_t pairs = std::min<int64_t>(tiles_r * tiles_c, dev->sms / 2);
+  return launch_dw2(p, ma, mdy, mo, static_cast<int>(2 * pairs), stream);
+}
+
 bool bad_dims(int64_t M, int64_t N, int64_t K) {
   return M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim;
 }
@@ -276,6 +301,8 @@ int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, in
   if (M == 0) return zero_fill(dW, K, N, stream);
   if (!A || !dY || !dW) return T3_EINVAL;
   if (M > kMaxInt8Reduction) return T3_EOVERFLOW;
+  const int st2 = run_dw2(A, dY, dW, M, N, K, stream);
+  if (st2 != T3_EINVAL) return st2;
   return run_tc<kOpDw>(reinterpret_cast<const uint8_t*>(A), M, K,
                        reinterpret_cast<const uint8_t*>(dY), M, N, dW, K, N, M,
                        tc::kChunkKbInt8, stream);

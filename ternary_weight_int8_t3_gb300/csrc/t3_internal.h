@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include "t3_tc_gemm.cuh"
 #include "t3_tc2.cuh"
+#include "t3_tc2_dw.cuh"
 
 namespace t3 {
 
@@ -29,6 +30,10 @@ int launch_tc2_fwd(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMa
                    const CUtensorMap& mo, int grid, cudaStream_t s);
 int launch_tc2_dx(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap& mw,
                   const CUtensorMap& mo, int grid, cudaStream_t s);
+
+// CTA-pair pipeline for dW (A, dY and dW all TMA-able).
+int launch_dw2(const dw2::Params& p, const CUtensorMap& ma, const CUtensorMap& mdy,
+               const CUtensorMap& mo, int grid, cudaStream_t s);
 
 // Small-M forward (M <= 32): zeroes C on `s`, then accumulates into it.
 int launch_skinny_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,

@@ -22,4 +22,21 @@ int launch_tc_dw(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap& 
   return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
 }
 
+int launch_dw2(const dw2::Params& p, const CUtensorMap& ma, const CUtensorMap& mdy,
+               const CUtensorMap& mo, int grid, cudaStream_t s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
+  static std::atomic<bool> attr_done[64];
+  if (dev < 0 || dev >= 64) return T3_EDEVICE;
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(dw2::dw2_kernel<dw2::kChunkElems>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dw2::SMEM_ALLOC) != cudaSuccess)
+      return T3_ECUDA;
+    attr_done[dev].store(true, std::memory_order_release);
+  }
+  dw2::dw2_kernel<dw2::kChunkElems><<<grid, dw2::kThreads, dw2::SMEM_ALLOC, s>>>(p, ma, mdy, mo);
+  return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
+}
+
 }  // namespace t3
