@@ -32,7 +32,9 @@
  *     stream reaches that point.  The library allocates no device memory per
  *     call.
  *   - Outputs are overwritten, never accumulated into.
- *   - A call with M, N or K equal to 0 does nothing and returns T3_OK.
+ *   - A call whose output is empty (no rows or no columns) does nothing and
+ *     returns T3_OK.  A call whose reduction is empty (K = 0 for the forward,
+ *     N = 0 for dX, M = 0 for dW) writes zeros to its output.
  *   - Argument errors are reported before anything is launched; nothing is
  *     written then.  No C++ exception crosses this interface and the device
  *     code never traps.
@@ -76,7 +78,10 @@ int t3_pack_ternary(const int8_t* w, uint8_t* wp, int64_t K, int64_t N);
  *   A [M][K], Wp [N][ceil(K/4)], C [M][N] (layouts above), device pointers.
  * Exact for every input when K <= 16777215 (|A W| <= 128 K fits int32);
  * larger K returns T3_EOVERFLOW.  M <= 32 takes the small-M path, which is
- * bound by reading the packed weights.
+ * bound by reading the packed weights: it enqueues two kernels on `stream`, one
+ * that zeroes C and one that adds the product into it; the second may start
+ * before the first ends (programmatic dependent launch) but touches C only
+ * after it, and the first touches C only after all earlier work on `stream`.
  */
 int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,
                 int64_t K, t3_stream_t stream);
@@ -109,7 +114,8 @@ const char* t3_status_string(int status);
  * `stream`, returns T3_ETIMEOUT if the word is set (T3_OK otherwise) and
  * clears it.  *detail, when not NULL, receives the recorded code (0 if none):
  * bits 0-7 the role that gave up (1 producer, 2 converter, 3 MMA issuer,
- * 4 epilogue), bits 8-15 the kernel (1 fwd, 2 dX, 3 dW, 4 small-M fwd).
+ * 4 epilogue, 5 pair forwarder), bits 8-15 the kernel (1 fwd, 2 dX, 3 dW on
+ * one CTA per tile; 4 small-M fwd; 5 fwd, 6 dX, 7 dW on CTA pairs).
  */
 int t3_last_device_error(t3_stream_t stream, int32_t* detail);
 
