@@ -233,6 +233,21 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand in the 128-byte
+// swizzle: atoms of 8 reduction rows x 128 B (64 f16 along MN); the leading
+// offset is the stride between atoms along MN, the stride offset the stride
+// between 8-row groups along the reduction (measured with a GPU probe).
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t addr, uint32_t mn_atom_stride,
+                                                       uint32_t group_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((mn_atom_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((group_stride >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor: f16 x f16 -> f32, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
   return (1u << 4)                                   // D format: f32

@@ -65,8 +65,10 @@ template <> struct RawW<kOpDx> { static constexpr int rows = BK, cols = 64; };  
 template <int OP> struct Layout {
   static constexpr int raw_w = RawW<OP>::rows * RawW<OP>::cols;
   static constexpr int raw_stage = ((RAW_A + raw_w) + 1023) / 1024 * 1024;
-  static constexpr int opb_atom = BNH * 128;          // [96 rows][64 f16]
-  static constexpr int opb_stage = 2 * opb_atom;      // two 64-element k atoms
+  static constexpr int opb_atom = BNH * 128;          // forward: [96 rows][64 f16]
+  // forward: two 64-element k atoms, K-major; dX: MN-major, per 8 n rows two
+  // 64-element k atoms (the CTA's 96 k fill one and a half)
+  static constexpr int opb_stage = (OP == kOpDx) ? (BK / 8) * 2048 : 2 * opb_atom;
   static constexpr int stage_out = 128 * 32 * 4;
   static constexpr int off_opb = 0;
   static constexpr int off_raw = off_opb + OP_STAGES * opb_stage;
@@ -224,41 +226,34 @@ __device__ __forceinline__ void decode_w_fwd(const uint8_t* raw_w, uint8_t* opb,
   }
 }
 
-// dX weights of CTA `rank`: packed [128 n][64 B = 256 k] (the pair uses k-local
-// [0, 192), this CTA [96 rank, 96 rank + 96)) -> f16 [96 k rows][128 n] as two
-// 64-n atoms.  Unit = (word column w of this CTA's 6, n group g of 16, byte
-// half bh): 8 packed words gathered, byte-transposed, decoded per k.  bh is
-// constant across each warp (units are numbered bh-major in blocks of 96).
+// dX weights of CTA `rank`, MN-major: packed [128 n][64 B = 256 k], of which
+// this CTA's 96 k are bytes [24 rank, 24 rank + 24) of every row -> f16
+// [n / 8][atom a][8 rows][128 B], atom a holding k in [64 a, 64 a + 64) of
+// the CTA's 96 (atom 1 half used), 16-B chunk q of row r at q ^ r.  Each unit
+// expands 8 codes (2 bytes) into one 16-B chunk with no transpose: the tensor
+// core reads the weights MN-major.  Units 0..1023 fill atom 0 (8 consecutive
+// threads = the 8 chunks of one row), units 1024..1535 atom 1 (8 consecutive
+// threads = chunks 0..3 of rows r and r + 4), so no store phase has a bank
+// conflict.
 __device__ __forceinline__ void decode_w_dx(const uint8_t* raw_w, uint8_t* opb, int tid,
                                             uint32_t rank) {
-  constexpr int kUnits = 6 * 16 * 2;
-  const uint32_t* rw = reinterpret_cast<const uint32_t*>(raw_w);
+  constexpr int kUnits = BK * 8 + BK * 4;
   for (int u = tid; u < kUnits; u += kWThreads) {
-    const int bh = u / 96, g = (u % 96) & 15, wl = (u % 96) >> 4;  // bh warp-uniform, wl < 6
-    const int wcol = 6 * static_cast<int>(rank) + wl;       // word column within the 64-B row
-    uint32_t x[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = rw[(8 * g + i) * 16 + wcol];
-    uint32_t Y[4], Z[4];
-    tc::transpose4x4(x[0], x[1], x[2], x[3], Y);
-    tc::transpose4x4(x[4], x[5], x[6], x[7], Z);
-    uint8_t* atom = opb + (g >> 3) * Layout<kOpDx>::opb_atom;
-    const int chunk = g & 7;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      if ((b >> 1) != bh) continue;  // warp-uniform split
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int krow = 16 * wl + 4 * b + j;
-        const uint32_t sy = Y[b] >> (2 * j), sz = Z[b] >> (2 * j);
-        uint4 o;
-        o.x = prmt(tc::kF16HiTable, 0u, ((sy << 4) & 0x3030u) | 0x0404u);
-        o.y = prmt(tc::kF16HiTable, 0u, ((sy >> 12) & 0x3030u) | 0x0404u);
-        o.z = prmt(tc::kF16HiTable, 0u, ((sz << 4) & 0x3030u) | 0x0404u);
-        o.w = prmt(tc::kF16HiTable, 0u, ((sz >> 12) & 0x3030u) | 0x0404u);
-        *reinterpret_cast<uint4*>(atom + tc::sw128(krow, chunk)) = o;
-      }
+    int n, q;
+    if (u < BK * 8) {
+      n = u >> 3;
+      q = u & 7;
+    } else {
+      const int v = u - BK * 8, t8 = v & 7, b = v >> 3;
+      n = ((b >> 2) << 3) + (b & 3) + ((t8 >> 2) << 2);
+      q = 8 + (t8 & 3);
     }
+    const uint32_t codes =
+        *reinterpret_cast<const uint16_t*>(raw_w + n * 64 + 24 * static_cast<int>(rank) + 2 * q);
+    const int r = n & 7;
+    *reinterpret_cast<uint4*>(opb + (n >> 3) * 2048 + (q >> 3) * 1024 + r * 128 +
+                              (((q & 7) ^ r) << 4)) =
+        tc::decode8_nibbles(tc::spread_codes_to_nibbles(codes));
   }
 }
 
@@ -409,7 +404,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------- MMA (even CTA)
     if (rank == 0 && lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(BMP, BN);
+      // the dX weights are MN-major (instruction-descriptor bit 16)
+      constexpr uint32_t idesc = idesc_f16_f32(BMP, BN) | (OP == kOpDx ? (1u << 16) : 0u);
       uint32_t os = 0, oph = 0, ab = 0, aph = 0;
       bool ok = true, issued_any = false;
       for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
@@ -427,9 +423,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t a0 = tmem_base + kActCol + os * (BK / 2);
 #pragma unroll
             for (int j = 0; j < BK / 16; ++j) {
-              umma_pair_ts(d_tmem, a0 + 8 * j,
-                           smem_desc_k_sw128(b0 + (j >> 2) * L::opb_atom + 32 * (j & 3)), idesc,
-                           (kb > c0 || j > 0) ? 1u : 0u);
+              // K-step j: forward weights K-major (atom j/4, 32 B further per
+              // step); dX weights MN-major (two 8-row n groups further per step)
+              const uint64_t bdesc =
+                  (OP == kOpDx)
+                      ? smem_desc_mn_sw128(b0 + j * 4096, 1024, 2048)
+                      : smem_desc_k_sw128(b0 + (j >> 2) * L::opb_atom + 32 * (j & 3));
+              umma_pair_ts(d_tmem, a0 + 8 * j, bdesc, idesc, (kb > c0 || j > 0) ? 1u : 0u);
             }
             issued_any = true;
             umma_commit_pair(&op_empty[os]);

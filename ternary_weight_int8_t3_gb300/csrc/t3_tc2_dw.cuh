@@ -92,17 +92,6 @@ __host__ __device__ constexpr uint32_t idesc_f16_mn(int m, int n) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);              // start address
-  d |= static_cast<uint64_t>((MN_ATOM >> 4) & 0x3FFFu) << 16;     // next atom along MN
-  d |= static_cast<uint64_t>((K_GROUP >> 4) & 0x3FFFu) << 32;     // next 8 rows along m
-  d |= static_cast<uint64_t>(1u) << 46;                           // descriptor version
-  d |= static_cast<uint64_t>(2u) << 61;                           // 128-byte swizzle
-  return d;
-}
-
 // One operand of one stage: raw int8 [64 m][128 MN] -> f16 MN-major atoms.
 // Unit u = (row m, 16-byte raw chunk c): 16 MN values -> two 8-value f16
 // chunks 2c, 2c+1 of atom c/4.  Threads c >= 4 write their odd chunk first so
@@ -273,8 +262,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t a0 = smem_addr(op + os * OP_STAGE);
-            const uint64_t adesc = smem_desc_mn_sw128(a0);
-            const uint64_t bdesc = smem_desc_mn_sw128(a0 + OP_OPERAND);
+            const uint64_t adesc = smem_desc_mn_sw128(a0, MN_ATOM, K_GROUP);
+            const uint64_t bdesc = smem_desc_mn_sw128(a0 + OP_OPERAND, MN_ATOM, K_GROUP);
             // K-step j covers m rows [16j, 16j + 16): two 8-row groups further on
 #pragma unroll
             for (int j = 0; j < BK / 16; ++j)
