@@ -22,6 +22,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// 16-byte shared-memory store as one st.shared.v4 (a 128-bit store per thread,
+// so that 8 threads with distinct 16-byte bank groups make one wavefront).
+__device__ __forceinline__ void sts128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(p)), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void sts128(void* p, const uint4& v) { sts128(p, v.x, v.y, v.z, v.w); }
+__device__ __forceinline__ void sts128(void* p, const int4& v) {
+  sts128(p, static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y), static_cast<uint32_t>(v.z),
+         static_cast<uint32_t>(v.w));
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -375,8 +375,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint4 hi, lo;
         act16_to_digits<kSigned>(xa[r], hi, lo);
         uint8_t* atom = bbuf + (c >> 3) * B_ATOM;
-        *reinterpret_cast<uint4*>(atom + tc::sw128(2 * ml, c & 7)) = hi;
-        *reinterpret_cast<uint4*>(atom + tc::sw128(2 * ml + 1, c & 7)) = lo;
+        sts128(atom + tc::sw128(2 * ml, c & 7), hi);
+        sts128(atom + tc::sw128(2 * ml + 1, c & 7), lo);
       }
       fence_proxy_async_smem();
       tc2::tmem_wait_st();

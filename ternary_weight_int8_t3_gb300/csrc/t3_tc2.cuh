@@ -218,10 +218,10 @@ __device__ __forceinline__ void decode_w_fwd(const uint8_t* raw_w, uint8_t* opb,
     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      *reinterpret_cast<uint4*>(atom + tc::sw128(row, 2 * w)) =
-          tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] & 0xFFFFu));
-      *reinterpret_cast<uint4*>(atom + tc::sw128(row, 2 * w + 1)) =
-          tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] >> 16));
+      sts128(atom + tc::sw128(row, 2 * w),
+             tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] & 0xFFFFu)));
+      sts128(atom + tc::sw128(row, 2 * w + 1),
+             tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] >> 16)));
     }
   }
 }
@@ -251,9 +251,8 @@ __device__ __forceinline__ void decode_w_dx(const uint8_t* raw_w, uint8_t* opb, 
     const uint32_t codes =
         *reinterpret_cast<const uint16_t*>(raw_w + n * 64 + 24 * static_cast<int>(rank) + 2 * q);
     const int r = n & 7;
-    *reinterpret_cast<uint4*>(opb + (n >> 3) * 2048 + (q >> 3) * 1024 + r * 128 +
-                              (((q & 7) ^ r) << 4)) =
-        tc::decode8_nibbles(tc::spread_codes_to_nibbles(codes));
+    sts128(opb + (n >> 3) * 2048 + (q >> 3) * 1024 + r * 128 + (((q & 7) ^ r) << 4),
+           tc::decode8_nibbles(tc::spread_codes_to_nibbles(codes)));
   }
 }
 
@@ -503,7 +502,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const int4 val =
                   make_int4(tc::f32_bits_to_i32(v[4 * c]), tc::f32_bits_to_i32(v[4 * c + 1]),
                             tc::f32_bits_to_i32(v[4 * c + 2]), tc::f32_bits_to_i32(v[4 * c + 3]));
-              *reinterpret_cast<int4*>(buf + tc::sw128(srow, c)) = val;
+              sts128(buf + tc::sw128(srow, c), val);
             }
             fence_proxy_async_smem();
             named_bar_sync(kEpiBarrier, 128);

@@ -111,11 +111,11 @@ __device__ __forceinline__ void widen_mn(const uint8_t* raw, uint8_t* op, int ti
     uint8_t* row = op + (m >> 3) * K_GROUP + (c >> 2) * MN_ATOM + r * 128;
     const int c0 = (2 * c) & 7, c1 = (2 * c + 1) & 7;
     if (c < 4) {
-      *reinterpret_cast<uint4*>(row + ((c0 ^ r) << 4)) = lo;
-      *reinterpret_cast<uint4*>(row + ((c1 ^ r) << 4)) = hi;
+      sts128(row + ((c0 ^ r) << 4), lo);
+      sts128(row + ((c1 ^ r) << 4), hi);
     } else {
-      *reinterpret_cast<uint4*>(row + ((c1 ^ r) << 4)) = hi;
-      *reinterpret_cast<uint4*>(row + ((c0 ^ r) << 4)) = lo;
+      sts128(row + ((c1 ^ r) << 4), hi);
+      sts128(row + ((c0 ^ r) << 4), lo);
     }
   }
 }
@@ -325,7 +325,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int4 val =
                 make_int4(tc::f32_bits_to_i32(v[4 * c]), tc::f32_bits_to_i32(v[4 * c + 1]),
                           tc::f32_bits_to_i32(v[4 * c + 2]), tc::f32_bits_to_i32(v[4 * c + 3]));
-            *reinterpret_cast<int4*>(buf + tc::sw128(srow, c)) = val;
+            sts128(buf + tc::sw128(srow, c), val);
           }
           fence_proxy_async_smem();
           named_bar_sync(kEpiBarrier, 128);
