@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-small-m", action="store_true",
                     help="skip the small-M forward sweep (for launch-list captures)")
+    ap.add_argument("--small-m-only", metavar="M,N,K", default=None,
+                    help="time one small-M forward configuration of the sweep and exit "
+                         "(for profiler captures)")
     return ap.parse_args()
 
 
@@ -178,14 +181,15 @@ def dram_traffic(product):
     return per.get(product)
 
 
-def bench_small_m(t3, torch, dev, stream, hbm_gbs, reps=30):
+def bench_small_m(t3, torch, dev, stream, hbm_gbs, reps=30, configs=None):
     """Small-M forward sweep: bytes moved (packed weights + activations + the
     int32 output) per call over its device time.  Enough distinct copies of Wp
     rotate through the calls that no copy is still in the 129 MB L2.  The calls
     are captured once in a CUDA graph and replayed, so the device time is not
-    hidden behind host launch overhead (a call is a memset of C plus one kernel)."""
+    hidden behind host launch overhead (a call is a kernel that zeroes C plus
+    the product kernel)."""
     out = []
-    for (m, n, k) in SMALL_M:
+    for (m, n, k) in (configs or SMALL_M):
         wl = t3_synth.BY_NAME[f"skinny_m{m}_n{n}_k{k}"]
         A, w, _ = t3_synth.make_inputs(wl)
         wp = t3.t3_pack_ternary(w)
@@ -312,6 +316,17 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
+
+    if args.small_m_only:
+        cfg = tuple(int(x) for x in args.small_m_only.split(","))
+        if cfg not in SMALL_M:
+            raise SystemExit(f"--small-m-only: {cfg} is not one of {SMALL_M}")
+        peaks, _ = read_peaks()
+        hbm = peaks.get("hbm_gbs", 6800.0)
+        calls = bench_small_m(t3, torch, dev, torch.cuda.current_stream(dev), hbm,
+                              configs=[cfg])
+        print(json.dumps({"small_m": {"hbm_peak_GBps": hbm, "calls": calls}}))
+        return
 
     A, w, dY = make_host_inputs()
     wp = t3.t3_pack_ternary(w)
