@@ -109,14 +109,14 @@ __device__ __forceinline__ void widen_mn(const uint8_t* raw, uint8_t* op, int ti
     tc::s8x4_to_f16(x.w, hi.z, hi.w);
     const int r = m & 7;
     uint8_t* row = op + (m >> 3) * K_GROUP + (c >> 2) * MN_ATOM + r * 128;
+    // selects, not a branch: a branch on c would split every warp and issue
+    // each store twice with half of the threads
+    const bool odd_first = c >= 4;
     const int c0 = (2 * c) & 7, c1 = (2 * c + 1) & 7;
-    if (c < 4) {
-      sts128(row + ((c0 ^ r) << 4), lo);
-      sts128(row + ((c1 ^ r) << 4), hi);
-    } else {
-      sts128(row + ((c1 ^ r) << 4), hi);
-      sts128(row + ((c0 ^ r) << 4), lo);
-    }
+    const int f = odd_first ? c1 : c0, g = odd_first ? c0 : c1;
+    const uint4 first = odd_first ? hi : lo, second = odd_first ? lo : hi;
+    sts128(row + ((f ^ r) << 4), first);
+    sts128(row + ((g ^ r) << 4), second);
   }
 }
 
