@@ -25,8 +25,9 @@
 // int32 by TMA bulk reduce-add (the first chunk of a tile is stored).
 //
 // Roles per CTA (704 threads): warps 0-7 convert A, warps 8-15 convert dY,
-// warp 16 is the TMA producer, warp 17 issues the MMAs (even CTA), warps 18-21
-// are the epilogue.
+// warp 16 is the TMA producer, warp 17 issues the MMAs (even CTA) or forwards
+// the odd CTA's "stage ready" to the even CTA with one cluster arrive per
+// stage, warps 18-21 are the epilogue.
 #pragma once
 #include <cstdint>
 #include "t3_tc2.cuh"
@@ -62,7 +63,7 @@ constexpr int OFF_OP = 0;
 constexpr int OFF_RAW = OFF_OP + OP_STAGES * OP_STAGE;
 constexpr int OFF_OUT = OFF_RAW + RAW_STAGES * RAW_STAGE;
 constexpr int OFF_BAR = OFF_OUT + 2 * STAGE_OUT;
-constexpr int N_BARS = 2 * RAW_STAGES + 2 * OP_STAGES + 2 * ACC_BUFS + 1;
+constexpr int N_BARS = 2 * RAW_STAGES + 3 * OP_STAGES + 2 * ACC_BUFS + 1;
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
 constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
@@ -138,7 +139,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* op_empty = op_full + OP_STAGES;     // both: MMA commit (multicast)
   uint64_t* acc_full = op_empty + OP_STAGES;    // both: MMA commit (multicast)
   uint64_t* acc_empty = acc_full + ACC_BUFS;    // even CTA: 4 epilogue warps x 2 CTAs
-  uint64_t* drain_bar = acc_empty + ACC_BUFS;
+  uint64_t* op_ready = acc_empty + ACC_BUFS;    // odd CTA: its converters, before forwarding
+  uint64_t* drain_bar = op_ready + OP_STAGES;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -155,7 +157,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&raw_empty[s], kConvWarps);
     }
     for (int s = 0; s < OP_STAGES; ++s) {
-      mbar_init(&op_full[s], 2 * kConvWarps);
+      mbar_init(&op_full[s], kConvWarps + 1);  // own converters + the odd CTA's forwarder
+      mbar_init(&op_ready[s], kConvWarps);
       mbar_init(&op_empty[s], 1);
     }
     for (int s = 0; s < ACC_BUFS; ++s) {
@@ -180,7 +183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- converters
     const bool a_warp = warp < kConvWarps / 2;
     const int htid = a_warp ? threadIdx.x : threadIdx.x - kHalfThreads;
-    const uint32_t op_full_leader0 = tc2::peer_addr(&op_full[0], 0);
+    uint64_t* signal = (rank == 0) ? op_full : op_ready;  // local, CTA scope
     uint32_t rs = 0, rph = 0, os = 0, oph = 0;
     bool ok = true;
     for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
@@ -195,12 +198,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&raw_empty[rs]);
-          // signal only: the operands stay in this SM's shared memory, fenced
-          // for the tensor core above
-          if (rank == 0)
-            mbar_arrive(&op_full[os]);
-          else
-            tc2::mbar_arrive_cluster_relaxed(op_full_leader0 + 8u * os);
+          mbar_arrive(&signal[os]);
         }
         if (++rs == RAW_STAGES) { rs = 0; rph ^= 1u; }
         if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
@@ -286,6 +284,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             : "memory");
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    if (rank == 1 && lane == 0) {
+      // forward each stage's readiness to the even CTA's MMA issuer: one
+      // signal-only cluster arrive per stage (the operands stay in this SM's
+      // shared memory, fenced for the tensor core by the converters)
+      const uint32_t op_full_leader0 = tc2::peer_addr(&op_full[0], 0);
+      uint32_t os = 0, oph = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+        for (int64_t kb = 0; kb < p.num_stages; ++kb) {
+          ok = mbar_wait(&op_ready[os], oph, abort_flag, p.err, code_base | 5);
+          if (!ok) break;
+          tc2::mbar_arrive_cluster_relaxed(op_full_leader0 + 8u * os);
+          if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
         }
       }
     }
