@@ -168,7 +168,7 @@ int run_tc2(const int8_t* act, const uint8_t* Wp, int32_t* out, int64_t M, int64
   if (!make_u8_map_tiled(&ma, act, M, act_cols, act_cols, 128, tc2::BK, true)) return T3_EINVAL;
   const bool w_ok = (OP == kOpFwd)
                         ? make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BNH, tc2::BK / 4)
-                        : make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BK, 64);
+                        : make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BK, tc2::BN / 4);
   if (!w_ok) return T3_EINVAL;
   if (!make_i32_map_tiled(&mo, out, M, out_cols, 128, 32, true)) return T3_EINVAL;
   tc2::Params p{};

@@ -60,7 +60,7 @@ constexpr int64_t kChunkStages = 65536 / BK;  // exact f32 chunk for ternary pro
 constexpr int RAW_A = 128 * BK;                 // [128 rows][128 B], 128-byte swizzle
 template <int OP> struct RawW;
 template <> struct RawW<kOpFwd> { static constexpr int rows = BNH, cols = BK / 4; };  // [96 n][32 B]
-template <> struct RawW<kOpDx> { static constexpr int rows = BK, cols = 64; };         // [128 n][64 B]
+template <> struct RawW<kOpDx> { static constexpr int rows = BK, cols = BN / 4; };     // [128 n][48 B]
 
 template <int OP> struct Layout {
   static constexpr int raw_w = RawW<OP>::rows * RawW<OP>::cols;
@@ -226,8 +226,9 @@ __device__ __forceinline__ void decode_w_fwd(const uint8_t* raw_w, uint8_t* opb,
   }
 }
 
-// dX weights of CTA `rank`, MN-major: packed [128 n][64 B = 256 k], of which
-// this CTA's 96 k are bytes [24 rank, 24 rank + 24) of every row -> f16
+// dX weights of CTA `rank`, MN-major: packed [128 n][48 B = the pair's 192 k],
+// of which this CTA's 96 k are bytes [24 rank, 24 rank + 24) of every row (the
+// 48-byte row stride also keeps the 2-byte loads free of bank conflicts) -> f16
 // [n / 8][atom a][8 rows][128 B], atom a holding k in [64 a, 64 a + 64) of
 // the CTA's 96 (atom 1 half used), 16-B chunk q of row r at q ^ r.  Each unit
 // expands 8 codes (2 bytes) into one 16-B chunk with no transpose: the tensor
@@ -249,7 +250,7 @@ __device__ __forceinline__ void decode_w_dx(const uint8_t* raw_w, uint8_t* opb, 
       q = 8 + (t8 & 3);
     }
     const uint32_t codes =
-        *reinterpret_cast<const uint16_t*>(raw_w + n * 64 + 24 * static_cast<int>(rank) + 2 * q);
+        *reinterpret_cast<const uint16_t*>(raw_w + n * (BN / 4) + 24 * static_cast<int>(rank) + 2 * q);
     const int r = n & 7;
     sts128(opb + (n >> 3) * 2048 + (q >> 3) * 1024 + r * 128 + (((q & 7) ^ r) << 4),
            tc::decode8_nibbles(tc::spread_codes_to_nibbles(codes)));
