@@ -276,6 +276,29 @@ def test_repeated_calls_same_result():
         assert np.array_equal(run_fwd(A, wp), first)
 
 
+def test_small_m_chained_calls_see_earlier_outputs():
+    """Back-to-back small-M calls on one stream, each reading the previous
+    call's output bytes as its input (activations, then packed weights): every
+    call must see the finished result of the one before it, whatever overlap
+    the launches allow."""
+    g = t3_synth.rng(21)
+    A0 = t3_synth.int8_uniform(g, (8, 1024))
+    wp0 = oracle.pack(t3_synth.ternary(g, (1024, 512)))
+    wp1 = oracle.pack(t3_synth.ternary(g, (2048, 300)))
+    A2 = t3_synth.int8_uniform(g, (5, 1600))
+    C0 = torch.empty((8, 512), dtype=torch.int32, device="cuda")
+    C1 = torch.empty((8, 300), dtype=torch.int32, device="cuda")
+    C2 = torch.empty((5, 24), dtype=torch.int32, device="cuda")
+    t3.t3_gemm_fwd(_dev(A0), _dev(wp0), K=1024, C=C0)
+    t3.t3_gemm_fwd(C0.view(torch.int8).view(8, 2048), _dev(wp1), K=2048, C=C1)
+    t3.t3_gemm_fwd(_dev(A2), C1.view(torch.uint8).view(24, 400), K=1600, C=C2)
+    torch.cuda.synchronize()
+    c0, c1, c2 = C0.cpu().numpy(), C1.cpu().numpy(), C2.cpu().numpy()
+    assert_same(c0, oracle.fwd(A0, wp0), "chained call 1")
+    assert_same(c1, oracle.fwd(c0.view(np.int8).reshape(8, 2048), wp1), "chained call 2")
+    assert_same(c2, oracle.fwd(A2, c1.view(np.uint8).reshape(24, 400)), "chained call 3")
+
+
 def test_empty_reduction_writes_zeros():
     C = torch.full((5, 7), 3, dtype=torch.int32, device="cuda")
     t3.t3_gemm_fwd(torch.empty((5, 0), dtype=torch.int8, device="cuda"),
