@@ -190,11 +190,16 @@ __device__ __forceinline__ void decode16_pairs(uint32_t x, uint32_t* o) {
 
 // ------------------------------------------------------------ converters
 
+// The dX converters work in two halves: *_load reads the raw bytes and converts
+// them into 32 registers as soon as the raw stage has landed, *_store writes
+// them once the operand slot is free, so that the conversion stays off the
+// path from the MMA's release of a slot to the slot's next use.  The forward
+// converts and stores in one pass (measured faster for its 10-stage tiles).
+
 // Activation row -> TMEM: thread (quadrant q, half h) owns lane q*32+lane and
 // reduction elements [64h, 64h+64) of the stage, in natural order.  The raw
 // tile is [128][128 B] in the 128-byte swizzle.
-__device__ __forceinline__ void act_to_tmem(const uint8_t* raw_a, uint32_t taddr, int row, int h) {
-  uint32_t v[32];
+__device__ __forceinline__ void act_load(const uint8_t* raw_a, int row, int h, uint32_t (&v)[32]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint4 x = *reinterpret_cast<const uint4*>(raw_a + tc::sw128(row, 4 * h + c));
@@ -203,26 +208,26 @@ __device__ __forceinline__ void act_to_tmem(const uint8_t* raw_a, uint32_t taddr
     tc::s8x4_to_f16(x.z, v[8 * c + 4], v[8 * c + 5]);
     tc::s8x4_to_f16(x.w, v[8 * c + 6], v[8 * c + 7]);
   }
-  tmem_st_32x32b_x32(taddr, v);
 }
 
 // Forward weights of this CTA: packed [96 n][32 B] -> f16 [96 n][128 k] as two
-// 64-k atoms, natural order.  Unit = (row, 16-byte half); rows vary fastest so
-// that each 8-thread store phase covers 8 rows.
+// 64-k atoms, natural order.  Unit = (row, 16-byte half), at most one per
+// thread; rows vary fastest so that each 8-thread store phase covers 8 rows.
+constexpr int kFwdUnits = BNH * 2;
+static_assert(kFwdUnits <= kWThreads, "one forward weight unit per thread");
+
 __device__ __forceinline__ void decode_w_fwd(const uint8_t* raw_w, uint8_t* opb, int tid) {
-  constexpr int kUnits = BNH * 2;
-  for (int u = tid; u < kUnits; u += kWThreads) {
-    const int row = u % BNH, h = u / BNH;
-    const uint4 x = *reinterpret_cast<const uint4*>(raw_w + row * 32 + 16 * h);
-    uint8_t* atom = opb + h * Layout<kOpFwd>::opb_atom;
-    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+  if (tid >= kFwdUnits) return;
+  const int row = tid % BNH, h = tid / BNH;
+  const uint4 x = *reinterpret_cast<const uint4*>(raw_w + row * 32 + 16 * h);
+  uint8_t* atom = opb + h * Layout<kOpFwd>::opb_atom;
+  const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      sts128(atom + tc::sw128(row, 2 * w),
-             tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] & 0xFFFFu)));
-      sts128(atom + tc::sw128(row, 2 * w + 1),
-             tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] >> 16)));
-    }
+  for (int w = 0; w < 4; ++w) {
+    sts128(atom + tc::sw128(row, 2 * w),
+           tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] & 0xFFFFu)));
+    sts128(atom + tc::sw128(row, 2 * w + 1),
+           tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] >> 16)));
   }
 }
 
@@ -235,25 +240,42 @@ __device__ __forceinline__ void decode_w_fwd(const uint8_t* raw_w, uint8_t* opb,
 // core reads the weights MN-major.  Units 0..1023 fill atom 0 (8 consecutive
 // threads = the 8 chunks of one row), units 1024..1535 atom 1 (8 consecutive
 // threads = chunks 0..3 of rows r and r + 4), so no store phase has a bank
-// conflict.
-__device__ __forceinline__ void decode_w_dx(const uint8_t* raw_w, uint8_t* opb, int tid,
-                                            uint32_t rank) {
-  constexpr int kUnits = BK * 8 + BK * 4;
-  for (int u = tid; u < kUnits; u += kWThreads) {
+// conflict.  Six units per thread.
+constexpr int kDxUnitsPerThread = (BK * 8 + BK * 4) / kWThreads;
+static_assert(kDxUnitsPerThread * 4 <= 32, "dX weight units fit the 32 staging registers");
+
+__device__ __forceinline__ void dx_unit(int u, int& n, int& q) {
+  if (u < BK * 8) {
+    n = u >> 3;
+    q = u & 7;
+  } else {
+    const int v = u - BK * 8, t8 = v & 7, b = v >> 3;
+    n = ((b >> 2) << 3) + (b & 3) + ((t8 >> 2) << 2);
+    q = 8 + (t8 & 3);
+  }
+}
+
+__device__ __forceinline__ void w_dx_load(const uint8_t* raw_w, int tid, uint32_t rank,
+                                          uint32_t (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < kDxUnitsPerThread; ++i) {
     int n, q;
-    if (u < BK * 8) {
-      n = u >> 3;
-      q = u & 7;
-    } else {
-      const int v = u - BK * 8, t8 = v & 7, b = v >> 3;
-      n = ((b >> 2) << 3) + (b & 3) + ((t8 >> 2) << 2);
-      q = 8 + (t8 & 3);
-    }
-    const uint32_t codes =
-        *reinterpret_cast<const uint16_t*>(raw_w + n * (BN / 4) + 24 * static_cast<int>(rank) + 2 * q);
+    dx_unit(tid + i * kWThreads, n, q);
+    const uint32_t codes = *reinterpret_cast<const uint16_t*>(
+        raw_w + n * (BN / 4) + 24 * static_cast<int>(rank) + 2 * q);
+    const uint4 o = tc::decode8_nibbles(tc::spread_codes_to_nibbles(codes));
+    v[4 * i] = o.x; v[4 * i + 1] = o.y; v[4 * i + 2] = o.z; v[4 * i + 3] = o.w;
+  }
+}
+
+__device__ __forceinline__ void w_dx_store(uint8_t* opb, int tid, const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < kDxUnitsPerThread; ++i) {
+    int n, q;
+    dx_unit(tid + i * kWThreads, n, q);
     const int r = n & 7;
-    sts128(opb + (n >> 3) * 2048 + (q >> 3) * 1024 + r * 128 + (((q & 7) ^ r) << 4),
-           tc::decode8_nibbles(tc::spread_codes_to_nibbles(codes)));
+    sts128(opb + (n >> 3) * 2048 + (q >> 3) * 1024 + r * 128 + (((q & 7) ^ r) << 4), v[4 * i],
+           v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
   }
 }
 
@@ -328,28 +350,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
       for (int64_t kb = 0; kb < p.num_stages; ++kb) {
-        ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2) &&
-             mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         const uint8_t* ra = raw + rs * L::raw_stage;
-        if (act_warp) {
-          act_to_tmem(ra, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kActCol +
-                              os * (BK / 2) + 32 * h,
-                      row, h);
-          tmem_wait_st();
-        } else if (OP == kOpFwd) {
-          decode_w_fwd(ra + RAW_A, opb + os * L::opb_stage, wtid);
-          fence_proxy_async_smem();
+        const uint32_t act_taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kActCol +
+                                   os * (BK / 2) + 32 * h;
+        if (OP == kOpFwd) {
+          ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2) &&
+               mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          if (act_warp) {
+            uint32_t v[32];
+            act_load(ra, row, h, v);
+            tmem_st_32x32b_x32(act_taddr, v);
+            tmem_wait_st();
+          } else {
+            decode_w_fwd(ra + RAW_A, opb + os * L::opb_stage, wtid);
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&raw_empty[rs]);
         } else {
-          decode_w_dx(ra + RAW_A, opb + os * L::opb_stage, wtid, rank);
-          fence_proxy_async_smem();
+          // dX converts as soon as the raw stage is in, releases it, and waits
+          // for the operand slot only before storing: its 27-stage tiles run
+          // latency-bound on the slot hand-off
+          ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          uint32_t v[32];
+          if (act_warp)
+            act_load(ra, row, h, v);
+          else
+            w_dx_load(ra + RAW_A, wtid, rank, v);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&raw_empty[rs]);
+          ok = mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          if (act_warp) {
+            tmem_st_32x32b_x32(act_taddr, v);
+            tmem_wait_st();
+          } else {
+            w_dx_store(opb + os * L::opb_stage, wtid, v);
+            fence_proxy_async_smem();
+          }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&raw_empty[rs]);
-          mbar_arrive(&signal[os]);
-        }
+        if (lane == 0) mbar_arrive(&signal[os]);
         if (++rs == RAW_STAGES) { rs = 0; rph ^= 1u; }
         if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
       }
