@@ -453,7 +453,7 @@ def main():
         "roofline": {"kernel": kname[dominant], "bound": "tensor", "achieved": op_tops[dominant],
                      "peak": peak, "unit": "TFLOP/s", "frac": op_tops[dominant] / peak,
                      "traffic": traffic, "peak_source": peak_note},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,  # fwd, dX, dW zeroing + dW product
         "e2e": {"value": 3 * OPS_PER_PRODUCT * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),

@@ -211,8 +211,13 @@ int run_dw2(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N
   if (tiles_r * tiles_c > kMaxDim) return T3_EINVAL;
   p.tiles_r = static_cast<int>(tiles_r);
   p.tiles_c = static_cast<int>(tiles_c);
+  p.num_chunks = static_cast<int>(ceil_div(M, dw2::kChunkElems));
   p.err = dev->err_word;
-  const int64_t pairs = std::min<int64_t>(tiles_r * tiles_c, dev->sms / 2);
+  // (tile, chunk) units, dealt evenly to at most one pair per two SMs
+  const int64_t units = tiles_r * tiles_c * p.num_chunks;
+  const int64_t pairs = std::min<int64_t>(units, std::max(dev->sms / 2, 1));
+  st = launch_zero_pdl(dW, K * N, dev->sms, stream);
+  if (st != T3_OK) return st;
   return launch_dw2(p, ma, mdy, mo, static_cast<int>(2 * pairs), stream);
 }
 

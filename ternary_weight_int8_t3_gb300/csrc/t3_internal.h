@@ -31,7 +31,13 @@ int launch_tc2_fwd(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMa
 int launch_tc2_dx(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap& mw,
                   const CUtensorMap& mo, int grid, cudaStream_t s);
 
-// CTA-pair pipeline for dW (A, dY and dW all TMA-able).
+// Zeroes out[0, n) on `s` as a programmatic dependent of the work before it:
+// it waits for that work to complete, then lets the next grid launch early.
+int launch_zero_pdl(int32_t* out, int64_t n, int sms, cudaStream_t s);
+
+// CTA-pair pipeline for dW (A, dY and dW all TMA-able).  Adds onto dW, which
+// launch_zero_pdl has cleared just before on `s`; launched as its programmatic
+// dependent.
 int launch_dw2(const dw2::Params& p, const CUtensorMap& ma, const CUtensorMap& mdy,
                const CUtensorMap& mo, int grid, cudaStream_t s);
 

@@ -164,6 +164,17 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (the tensor core reading operands).
+// Waits until the grids this one depends on programmatically have completed
+// and their writes are visible; a no-op without such a dependency.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the programmatically dependent grid launch before this one finishes.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

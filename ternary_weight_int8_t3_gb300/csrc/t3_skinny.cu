@@ -131,17 +131,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&v)
       : "r"(taddr));
 }
 
-// Waits until the grids this one depends on programmatically have completed
-// and their writes are visible; a no-op without such a dependency.
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// Lets the programmatically dependent grid launch before this one finishes.
-__device__ __forceinline__ void launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // e4m3 weight of code c = byte c of this word: 0 -> 0x00, 1 -> 0x38 (+1.0),
 // 2 -> 0xB8 (-1.0), 3 -> 0x00.
 constexpr uint32_t kE4m3Table = 0x00B83800u;
@@ -617,7 +606,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // Zeroes C ([n] int32).  Launched as a programmatic dependent of whatever
 // precedes it, so that its launch overlaps that grid's tail: it waits for that
 // grid to complete before anything else, then lets the product kernel launch.
-__global__ void __launch_bounds__(256) skinny_zero_kernel(int32_t* C, int64_t n) {
+__global__ void __launch_bounds__(256) zero_kernel_pdl(int32_t* C, int64_t n) {
   grid_dependency_wait();
   launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -633,6 +622,23 @@ __global__ void __launch_bounds__(256) skinny_zero_kernel(int32_t* C, int64_t n)
 }
 
 }  // namespace sk
+
+int launch_zero_pdl(int32_t* out, int64_t n, int sms, cudaStream_t s) {
+  int64_t zgrid = (n / 4 + 255) / 256;
+  if (zgrid < 1) zgrid = 1;
+  if (zgrid > 2 * sms) zgrid = 2 * sms;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t zcfg = {};
+  zcfg.gridDim = dim3(static_cast<unsigned>(zgrid), 1, 1);
+  zcfg.blockDim = dim3(256, 1, 1);
+  zcfg.stream = s;
+  zcfg.attrs = attr;
+  zcfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&zcfg, sk::zero_kernel_pdl, out, n) == cudaSuccess ? T3_OK
+                                                                                : T3_ECUDA;
+}
 
 int launch_skinny_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,
                       int64_t K, int sms, int* err, cudaStream_t s) {
@@ -676,20 +682,11 @@ int launch_skinny_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M,
     attr_done[dev].store(true, std::memory_order_release);
   }
 
-  const int64_t total = M * N;
-  int64_t zgrid = (total / 4 + 255) / 256;
-  if (zgrid < 1) zgrid = 1;
-  if (zgrid > 2 * sms) zgrid = 2 * sms;
+  const int zst = launch_zero_pdl(C, M * N, sms, s);
+  if (zst != T3_OK) return zst;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t zcfg = {};
-  zcfg.gridDim = dim3(static_cast<unsigned>(zgrid), 1, 1);
-  zcfg.blockDim = dim3(256, 1, 1);
-  zcfg.stream = s;
-  zcfg.attrs = attr;
-  zcfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&zcfg, sk::skinny_zero_kernel, C, total) != cudaSuccess) return T3_ECUDA;
 
   const int64_t max_pairs = sms / 2 > 0 ? sms / 2 : 1;
   const int npairs = static_cast<int>(units < max_pairs ? units : max_pairs);

@@ -22,7 +22,12 @@
 // (1 KB here), its stride offset the stride between 8-row groups along m (2 KB).
 // Exactness: each product is at most 2^14 in magnitude, so a chunk of 1024
 // reduction elements sums to at most 2^24 in f32, exactly; chunks are added in
-// int32 by TMA bulk reduce-add (the first chunk of a tile is stored).
+// int32 by TMA bulk reduce-add onto an output that a zeroing grid cleared.
+// Work units are (tile, chunk) pairs, numbered tile-major and dealt to the CTA
+// pairs in equal contiguous ranges: 70 tiles x 16 chunks of the layer above
+// give every pair 14 or 15 units instead of one whole tile to 70 of 76 pairs.
+// A pair takes its units chunk-first, so that all pairs sweep the reduction
+// together and the inputs they read at one time stay few.
 //
 // Roles per CTA (704 threads): warps 0-7 convert A, warps 8-15 convert dY,
 // warp 16 is the TMA producer, warp 17 issues the MMAs (even CTA) or forwards
@@ -72,7 +77,26 @@ struct Params {
   int64_t M, N, K;       // the product's sizes: reduction M, dW [K][N]
   int64_t num_stages;    // stages along the reduction
   int tiles_r, tiles_c;  // tiles along k, along n
+  int num_chunks;        // exact chunks along the reduction
   int* err;
+};
+
+// The (tile, chunk) units of one CTA pair: tile-major numbers [u0, u1).
+struct Units {
+  int64_t u0, u1;
+  int nc, t0, t1;
+  __device__ __forceinline__ Units(const Params& p, int pair, int npairs) {
+    nc = p.num_chunks;
+    const int64_t total = static_cast<int64_t>(p.tiles_r) * p.tiles_c * nc;
+    u0 = total * pair / npairs;
+    u1 = total * (pair + 1) / npairs;
+    t0 = static_cast<int>(u0 / nc);
+    t1 = static_cast<int>((u1 - 1) / nc);
+  }
+  __device__ __forceinline__ bool has(int t, int c) const {
+    const int64_t u = static_cast<int64_t>(t) * nc + c;
+    return u >= u0 && u < u1;
+  }
 };
 
 // D (both CTAs' TMEM) (+)= A (both CTAs' shared memory) x B (both CTAs' shared
@@ -147,7 +171,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = tc2::cluster_rank();
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int num_tiles = p.tiles_r * p.tiles_c;
+  const Units units(p, pair, npairs);
   constexpr int64_t kChunkStages = CHUNK / BK;
   constexpr int code_base = 7 << 8;
 
@@ -186,8 +210,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t* signal = (rank == 0) ? op_full : op_ready;  // local, CTA scope
     uint32_t rs = 0, rph = 0, os = 0, oph = 0;
     bool ok = true;
-    for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
-      for (int64_t kb = 0; kb < p.num_stages; ++kb) {
+    for (int c = 0; ok && c < units.nc; ++c)
+    for (int tile = units.t0; ok && tile <= units.t1; ++tile) {
+      if (!units.has(tile, c)) continue;
+      const int64_t k1 = min(p.num_stages, (c + 1) * kChunkStages);
+      for (int64_t kb = c * kChunkStages; kb < k1; ++kb) {
         ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2) &&
              mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -212,11 +239,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
     bool ok = true;
-    for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+    for (int c = 0; ok && c < units.nc; ++c)
+    for (int tile = units.t0; ok && tile <= units.t1; ++tile) {
+      if (!units.has(tile, c)) continue;
       const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
       const int ax = tr * BMP + static_cast<int>(rank) * 128;    // k of this CTA's A rows
       const int bx = tcol * BN + static_cast<int>(rank) * BNH;   // n of this CTA's dY rows
-      for (int64_t kb = 0; kb < p.num_stages; ++kb) {
+      const int64_t k1 = min(p.num_stages, (c + 1) * kChunkStages);
+      for (int64_t kb = c * kChunkStages; kb < k1; ++kb) {
         if (lane == 0)
           ok = mbar_wait(&raw_empty[stage], phase ^ 1u, abort_flag, p.err, code_base | 1);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -248,9 +278,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_f16_mn(BMP, BN);
       uint32_t os = 0, oph = 0, ab = 0, aph = 0;
       bool ok = true, issued_any = false;
-      for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
-        for (int64_t c0 = 0; ok && c0 < p.num_stages; c0 += kChunkStages) {
-          const int64_t c1 = (p.num_stages < c0 + kChunkStages) ? p.num_stages : c0 + kChunkStages;
+      for (int c = 0; ok && c < units.nc; ++c)
+      for (int tile = units.t0; ok && tile <= units.t1; ++tile) {
+        if (!units.has(tile, c)) continue;
+        {
+          const int64_t c0 = c * kChunkStages;
+          const int64_t c1 = min(p.num_stages, c0 + kChunkStages);
           ok = mbar_wait(&acc_empty[ab], aph ^ 1u, abort_flag, p.err, code_base | 3);
           if (!ok) break;
           tc_fence_after();
@@ -294,8 +327,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t op_full_leader0 = tc2::peer_addr(&op_full[0], 0);
       uint32_t os = 0, oph = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
-        for (int64_t kb = 0; kb < p.num_stages; ++kb) {
+      for (int c = 0; ok && c < units.nc; ++c)
+      for (int tile = units.t0; ok && tile <= units.t1; ++tile) {
+        if (!units.has(tile, c)) continue;
+        const int64_t k1 = min(p.num_stages, (c + 1) * kChunkStages);
+        for (int64_t kb = c * kChunkStages; kb < k1; ++kb) {
           ok = mbar_wait(&op_ready[os], oph, abort_flag, p.err, code_base | 5);
           if (!ok) break;
           tc2::mbar_arrive_cluster_relaxed(op_full_leader0 + 8u * os);
@@ -313,17 +349,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t ab = 0, aph = 0, slab = 0;
     bool ok = true;
     if (epi_tid == 0) prefetch_tensormap(&map_out);
-    for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+    // every unit adds onto the output: the zeroing grid must have completed
+    grid_dependency_wait();
+    for (int c = 0; ok && c < units.nc; ++c)
+    for (int tile = units.t0; ok && tile <= units.t1; ++tile) {
+      if (!units.has(tile, c)) continue;
       const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
       const int row0 = tr * BMP + static_cast<int>(rank) * 128;
-      for (int64_t c0 = 0; c0 < p.num_stages; c0 += kChunkStages) {
+      {
         ok = mbar_wait(&acc_full[ab], aph, abort_flag, p.err, code_base | 4);
         ok = named_bar_and(kEpiBarrier, 128, __all_sync(0xffffffffu, ok));
         if (!ok) break;
         tc_fence_after();
-        const bool first = (c0 == 0);
-        // a later chunk adds onto what the first chunk stored
-        if (c0 == kChunkStages && epi_tid == 0) bulk_wait_group<0>();
         for (int cb = 0; cb < BN / 32; ++cb) {
           const int64_t col0 = static_cast<int64_t>(tcol) * BN + cb * 32;
           if (col0 >= p.N) break;
@@ -344,10 +381,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           named_bar_sync(kEpiBarrier, 128);
           if (epi_tid == 0 && row0 < p.K) {  // a tile half wholly past K writes nothing
-            if (first)
-              tma_store_2d(&map_out, buf, static_cast<int>(col0), row0);
-            else
-              tma_reduce_add_2d(&map_out, buf, static_cast<int>(col0), row0);
+            tma_reduce_add_2d(&map_out, buf, static_cast<int>(col0), row0);
             bulk_commit_group();
           }
           ++slab;

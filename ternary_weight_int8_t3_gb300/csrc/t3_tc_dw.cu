@@ -35,7 +35,18 @@ int launch_dw2(const dw2::Params& p, const CUtensorMap& ma, const CUtensorMap& m
       return T3_ECUDA;
     attr_done[dev].store(true, std::memory_order_release);
   }
-  dw2::dw2_kernel<dw2::kChunkElems><<<grid, dw2::kThreads, dw2::SMEM_ALLOC, s>>>(p, ma, mdy, mo);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(dw2::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = dw2::SMEM_ALLOC;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, dw2::dw2_kernel<dw2::kChunkElems>, p, ma, mdy, mo) != cudaSuccess)
+    return T3_ECUDA;
   return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
 }
 
