@@ -99,6 +99,10 @@ int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, 
  *   A [M][K], dY [M][N], dW [K][N].
  * int8 x int8 products reach 16384, so the reduction is exact in int32 only
  * for M <= 131071 (the pages' bound); larger M returns T3_EOVERFLOW.
+ * When every operand is TMA-addressable (16-byte aligned bases, N and K
+ * multiples of 16) it enqueues two kernels on `stream`: one that zeroes dW and
+ * one that adds 1024-row partial sums into it, with the same ordering as the
+ * small-M forward above; otherwise one kernel that writes dW.
  */
 int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N,
                    int64_t K, t3_stream_t stream);
