@@ -190,6 +190,14 @@ __device__ __forceinline__ void decode16_pairs(uint32_t x, uint32_t* o) {
 
 // ------------------------------------------------------------ converters
 
+// Four int8 b0..b3 -> f16x2 words (b0, b2) and (b1, b3), exact (same bias
+// trick as tc::s8x4_to_f16, other byte pairs).
+__device__ __forceinline__ void s8x4_to_f16_evenodd(uint32_t x, uint32_t& even, uint32_t& odd) {
+  const uint32_t y = x ^ 0x80808080u;
+  even = hsub2(prmt(y, 0x64646464u, 0x4240u), 0x64806480u);
+  odd = hsub2(prmt(y, 0x64646464u, 0x4341u), 0x64806480u);
+}
+
 // The dX converters work in two halves: *_load reads the raw bytes and converts
 // them into 32 registers as soon as the raw stage has landed, *_store writes
 // them once the operand slot is free, so that the conversion stays off the
@@ -197,37 +205,58 @@ __device__ __forceinline__ void decode16_pairs(uint32_t x, uint32_t* o) {
 // converts and stores in one pass (measured faster for its 10-stage tiles).
 
 // Activation row -> TMEM: thread (quadrant q, half h) owns lane q*32+lane and
-// reduction elements [64h, 64h+64) of the stage, in natural order.  The raw
-// tile is [128][128 B] in the 128-byte swizzle.
+// reduction elements [64h, 64h+64) of the stage.  The raw tile is [128][128 B]
+// in the 128-byte swizzle.  kEvenOdd: within every 16 reduction elements the
+// even ones come first, then the odd ones -- the order in which the forward's
+// weight decode (decode_w_fwd) emits its codes; both operands of the forward
+// use it, so the products and their sum are unchanged.  Otherwise natural order.
+template <bool kEvenOdd>
 __device__ __forceinline__ void act_load(const uint8_t* raw_a, int row, int h, uint32_t (&v)[32]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint4 x = *reinterpret_cast<const uint4*>(raw_a + tc::sw128(row, 4 * h + c));
-    tc::s8x4_to_f16(x.x, v[8 * c + 0], v[8 * c + 1]);
-    tc::s8x4_to_f16(x.y, v[8 * c + 2], v[8 * c + 3]);
-    tc::s8x4_to_f16(x.z, v[8 * c + 4], v[8 * c + 5]);
-    tc::s8x4_to_f16(x.w, v[8 * c + 6], v[8 * c + 7]);
+    if (kEvenOdd) {
+      s8x4_to_f16_evenodd(x.x, v[8 * c + 0], v[8 * c + 4]);
+      s8x4_to_f16_evenodd(x.y, v[8 * c + 1], v[8 * c + 5]);
+      s8x4_to_f16_evenodd(x.z, v[8 * c + 2], v[8 * c + 6]);
+      s8x4_to_f16_evenodd(x.w, v[8 * c + 3], v[8 * c + 7]);
+    } else {
+      tc::s8x4_to_f16(x.x, v[8 * c + 0], v[8 * c + 1]);
+      tc::s8x4_to_f16(x.y, v[8 * c + 2], v[8 * c + 3]);
+      tc::s8x4_to_f16(x.z, v[8 * c + 4], v[8 * c + 5]);
+      tc::s8x4_to_f16(x.w, v[8 * c + 6], v[8 * c + 7]);
+    }
   }
 }
 
 // Forward weights of this CTA: packed [96 n][32 B] -> f16 [96 n][128 k] as two
-// 64-k atoms, natural order.  Unit = (row, 16-byte half), at most one per
-// thread; rows vary fastest so that each 8-thread store phase covers 8 rows.
-constexpr int kFwdUnits = BNH * 2;
-static_assert(kFwdUnits <= kWThreads, "one forward weight unit per thread");
+// 64-k atoms.  Unit = (row, 32-bit word of 16 codes): 768 units, exactly three
+// per weight thread, so that every weight warp (two per warp scheduler) does
+// the same share -- the decode is issue-bound.  Rows vary fastest, so each
+// 8-thread store phase covers 8 rows.  A word's 16 codes go out as two 16-byte
+// chunks, even codes then odd codes (the order act_load<true> writes the
+// activations in): masking the word with 0x33333333 leaves code 2j in nibble
+// j, ready as a byte-permute selector into the f16 high-byte table, without
+// spreading the codes first.
+constexpr int kFwdWordUnits = BNH * (BK / 16);
+static_assert(kFwdWordUnits % kWThreads == 0, "equal forward weight share per thread");
 
 __device__ __forceinline__ void decode_w_fwd(const uint8_t* raw_w, uint8_t* opb, int tid) {
-  if (tid >= kFwdUnits) return;
-  const int row = tid % BNH, h = tid / BNH;
-  const uint4 x = *reinterpret_cast<const uint4*>(raw_w + row * 32 + 16 * h);
-  uint8_t* atom = opb + h * Layout<kOpFwd>::opb_atom;
-  const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    sts128(atom + tc::sw128(row, 2 * w),
-           tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] & 0xFFFFu)));
-    sts128(atom + tc::sw128(row, 2 * w + 1),
-           tc::decode8_nibbles(tc::spread_codes_to_nibbles(xs[w] >> 16)));
+  for (int i = 0; i < kFwdWordUnits / kWThreads; ++i) {
+    const int u = tid + i * kWThreads;
+    const int row = u % BNH, w = u / BNH;
+    const uint32_t x = *reinterpret_cast<const uint32_t*>(raw_w + row * 32 + 4 * w);
+    const uint32_t e = x & 0x33333333u, o = (x >> 2) & 0x33333333u;
+    const uint32_t he0 = prmt(tc::kF16HiTable, 0u, e);
+    const uint32_t he1 = prmt(tc::kF16HiTable, 0u, e >> 16);
+    const uint32_t ho0 = prmt(tc::kF16HiTable, 0u, o);
+    const uint32_t ho1 = prmt(tc::kF16HiTable, 0u, o >> 16);
+    uint8_t* atom = opb + (w >> 2) * Layout<kOpFwd>::opb_atom;
+    sts128(atom + tc::sw128(row, 2 * (w & 3)), prmt(he0, 0u, 0x1404u),
+           prmt(he0, 0u, 0x3424u), prmt(he1, 0u, 0x1404u), prmt(he1, 0u, 0x3424u));
+    sts128(atom + tc::sw128(row, 2 * (w & 3) + 1), prmt(ho0, 0u, 0x1404u),
+           prmt(ho0, 0u, 0x3424u), prmt(ho1, 0u, 0x1404u), prmt(ho1, 0u, 0x3424u));
   }
 }
 
@@ -359,7 +388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           if (act_warp) {
             uint32_t v[32];
-            act_load(ra, row, h, v);
+            act_load<true>(ra, row, h, v);
             tmem_st_32x32b_x32(act_taddr, v);
             tmem_wait_st();
           } else {
@@ -376,7 +405,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           uint32_t v[32];
           if (act_warp)
-            act_load(ra, row, h, v);
+            act_load<false>(ra, row, h, v);
           else
             w_dx_load(ra + RAW_A, wtid, rank, v);
           __syncwarp();
