@@ -261,50 +261,60 @@ __device__ __forceinline__ void decode_w_fwd(const uint8_t* raw_w, uint8_t* opb,
 }
 
 // dX weights of CTA `rank`, MN-major: packed [128 n][48 B = the pair's 192 k],
-// of which this CTA's 96 k are bytes [24 rank, 24 rank + 24) of every row (the
-// 48-byte row stride also keeps the 2-byte loads free of bank conflicts) -> f16
-// [n / 8][atom a][8 rows][128 B], atom a holding k in [64 a, 64 a + 64) of
-// the CTA's 96 (atom 1 half used), 16-B chunk q of row r at q ^ r.  Each unit
-// expands 8 codes (2 bytes) into one 16-B chunk with no transpose: the tensor
-// core reads the weights MN-major.  Units 0..1023 fill atom 0 (8 consecutive
-// threads = the 8 chunks of one row), units 1024..1535 atom 1 (8 consecutive
-// threads = chunks 0..3 of rows r and r + 4), so no store phase has a bank
-// conflict.  Six units per thread.
-constexpr int kDxUnitsPerThread = (BK * 8 + BK * 4) / kWThreads;
-static_assert(kDxUnitsPerThread * 4 <= 32, "dX weight units fit the 32 staging registers");
+// of which this CTA's 96 k are bytes [24 rank, 24 rank + 24) of every row ->
+// f16 [n / 8][atom a][8 rows][128 B], atom a holding k in [64 a, 64 a + 64) of
+// the CTA's 96 (atom 1 half used), 16-B chunk q of row r at q ^ r.  No
+// transpose: the tensor core reads the weights MN-major.  Unit = (row n, word j
+// of 16 codes = k in [16 j, 16 j + 16)): 768 units, three per weight thread,
+// rows varying fastest so that each 8-thread store phase covers 8 rows.  A
+// word goes out as chunk 2j (its even codes) and chunk 2j + 1 (its odd codes),
+// like the forward's decode; here that permutes the MMA's N columns within
+// every 16, and the epilogue puts them back (dx_column).
+constexpr int kDxWordUnits = BK * (BN / 2 / 16);
+static_assert(kDxWordUnits % kWThreads == 0, "equal dX weight share per thread");
+constexpr int kDxWordsPerThread = kDxWordUnits / kWThreads;
+static_assert(kDxWordsPerThread * 8 <= 32, "dX weight units fit the 32 staging registers");
 
-__device__ __forceinline__ void dx_unit(int u, int& n, int& q) {
-  if (u < BK * 8) {
-    n = u >> 3;
-    q = u & 7;
-  } else {
-    const int v = u - BK * 8, t8 = v & 7, b = v >> 3;
-    n = ((b >> 2) << 3) + (b & 3) + ((t8 >> 2) << 2);
-    q = 8 + (t8 & 3);
-  }
+// Accumulator column holding output column e of a 32-column block.
+__host__ __device__ constexpr int dx_column(int e) {
+  return (e & 16) | ((e & 1) << 3) | ((e & 15) >> 1);
 }
 
 __device__ __forceinline__ void w_dx_load(const uint8_t* raw_w, int tid, uint32_t rank,
                                           uint32_t (&v)[32]) {
 #pragma unroll
-  for (int i = 0; i < kDxUnitsPerThread; ++i) {
-    int n, q;
-    dx_unit(tid + i * kWThreads, n, q);
-    const uint32_t codes = *reinterpret_cast<const uint16_t*>(
-        raw_w + n * (BN / 4) + 24 * static_cast<int>(rank) + 2 * q);
-    const uint4 o = tc::decode8_nibbles(tc::spread_codes_to_nibbles(codes));
-    v[4 * i] = o.x; v[4 * i + 1] = o.y; v[4 * i + 2] = o.z; v[4 * i + 3] = o.w;
+  for (int i = 0; i < kDxWordsPerThread; ++i) {
+    const int u = tid + i * kWThreads;
+    const int n = u % BK, j = u / BK;
+    const uint32_t x = *reinterpret_cast<const uint32_t*>(
+        raw_w + n * (BN / 4) + 24 * static_cast<int>(rank) + 4 * j);
+    const uint32_t e = x & 0x33333333u, o = (x >> 2) & 0x33333333u;
+    const uint32_t he0 = prmt(tc::kF16HiTable, 0u, e);
+    const uint32_t he1 = prmt(tc::kF16HiTable, 0u, e >> 16);
+    const uint32_t ho0 = prmt(tc::kF16HiTable, 0u, o);
+    const uint32_t ho1 = prmt(tc::kF16HiTable, 0u, o >> 16);
+    v[8 * i + 0] = prmt(he0, 0u, 0x1404u);
+    v[8 * i + 1] = prmt(he0, 0u, 0x3424u);
+    v[8 * i + 2] = prmt(he1, 0u, 0x1404u);
+    v[8 * i + 3] = prmt(he1, 0u, 0x3424u);
+    v[8 * i + 4] = prmt(ho0, 0u, 0x1404u);
+    v[8 * i + 5] = prmt(ho0, 0u, 0x3424u);
+    v[8 * i + 6] = prmt(ho1, 0u, 0x1404u);
+    v[8 * i + 7] = prmt(ho1, 0u, 0x3424u);
   }
 }
 
 __device__ __forceinline__ void w_dx_store(uint8_t* opb, int tid, const uint32_t (&v)[32]) {
 #pragma unroll
-  for (int i = 0; i < kDxUnitsPerThread; ++i) {
-    int n, q;
-    dx_unit(tid + i * kWThreads, n, q);
-    const int r = n & 7;
-    sts128(opb + (n >> 3) * 2048 + (q >> 3) * 1024 + r * 128 + (((q & 7) ^ r) << 4), v[4 * i],
-           v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  for (int i = 0; i < kDxWordsPerThread; ++i) {
+    const int u = tid + i * kWThreads;
+    const int n = u % BK, j = u / BK, r = n & 7;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int q = 2 * j + h;
+      sts128(opb + (n >> 3) * 2048 + (q >> 3) * 1024 + r * 128 + (((q & 7) ^ r) << 4),
+             v[8 * i + 4 * h], v[8 * i + 4 * h + 1], v[8 * i + 4 * h + 2], v[8 * i + 4 * h + 3]);
+    }
   }
 }
 
@@ -567,6 +577,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                  cb * 32,
                              v);
           tmem_wait_ld();
+          if (OP == kOpDx) {  // undo the weight decode's column order
+            uint32_t t[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) t[e] = v[dx_column(e)];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = t[e];
+          }
           if (p.use_tma_out) {
             uint8_t* buf = stage_out + (slab & 1) * L::stage_out;
             if (epi_tid == 0) bulk_wait_group_read<1>();
