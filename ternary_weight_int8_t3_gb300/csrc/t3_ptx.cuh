@@ -73,13 +73,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits until the phase with the given parity has completed.  Bounded: on
 // timeout (or when another role of the CTA has aborted) it records `code` in
 // *err (first writer wins), raises *abort_flag and returns false.
+// As mbar_try_wait, but the thread may stay suspended up to `hint_ns` waiting
+// for the phase instead of returning at once (fewer shared-memory polls).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag, int* err, int code) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = global_timer_ns();
   for (uint32_t spin = 1;; ++spin) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((spin & 255u) == 0) {
+    if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;
+    if ((spin & 15u) == 0) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
         atomicCAS(err, 0, code);
