@@ -230,22 +230,28 @@ __device__ __forceinline__ void act_load(const uint8_t* raw_a, int row, int h, u
 }
 
 // Forward weights of this CTA: packed [96 n][32 B] -> f16 [96 n][128 k] as two
-// 64-k atoms.  Unit = (row, 32-bit word of 16 codes): 768 units, exactly three
-// per weight thread, so that every weight warp (two per warp scheduler) does
-// the same share -- the decode is issue-bound.  Rows vary fastest, so each
-// 8-thread store phase covers 8 rows.  A word's 16 codes go out as two 16-byte
-// chunks, even codes then odd codes (the order act_load<true> writes the
-// activations in): masking the word with 0x33333333 leaves code 2j in nibble
-// j, ready as a byte-permute selector into the f16 high-byte table, without
-// spreading the codes first.
+// 64-k atoms.  Unit = (row, 32-bit word w of 16 codes): 768 units, exactly
+// three per weight thread, so that every weight warp (two per warp scheduler)
+// does the same share -- the decode is issue-bound.  A word's 16 codes go out
+// as two 16-byte chunks, even codes then odd codes (the order act_load<true>
+// writes the activations in): masking the word with 0x33333333 leaves code 2j
+// in nibble j, ready as a byte-permute selector into the f16 high-byte table,
+// without spreading the codes first.
+// Lanes: one warp instruction covers rows 4g .. 4g+3 x words 0..7, so its 32
+// word loads (row stride 32 B) hit 32 distinct banks, and each 8-lane store
+// phase (two rows of opposite parity x words 0..3 or 4..7) hits 8 distinct
+// 16-byte bank groups of the swizzled rows.
 constexpr int kFwdWordUnits = BNH * (BK / 16);
-static_assert(kFwdWordUnits % kWThreads == 0, "equal forward weight share per thread");
+static_assert(kFwdWordUnits % kWThreads == 0 && BNH % 4 == 0, "equal forward weight share");
+constexpr int kFwdWordsPerThread = kFwdWordUnits / kWThreads;
 
 __device__ __forceinline__ void decode_w_fwd(const uint8_t* raw_w, uint8_t* opb, int tid) {
+  const int wl = tid & 31, wwarp = tid >> 5;
 #pragma unroll
-  for (int i = 0; i < kFwdWordUnits / kWThreads; ++i) {
-    const int u = tid + i * kWThreads;
-    const int row = u % BNH, w = u / BNH;
+  for (int i = 0; i < kFwdWordsPerThread; ++i) {
+    const int g = i * (kWThreads / 32) + wwarp;  // group of four rows
+    const int row = 4 * g + ((wl >> 2) & 1) + 2 * ((wl >> 3) & 1);
+    const int w = (wl & 3) + 4 * (wl >> 4);
     const uint32_t x = *reinterpret_cast<const uint32_t*>(raw_w + row * 32 + 4 * w);
     const uint32_t e = x & 0x33333333u, o = (x >> 2) & 0x33333333u;
     const uint32_t he0 = prmt(tc::kF16HiTable, 0u, e);
@@ -265,15 +271,25 @@ __device__ __forceinline__ void decode_w_fwd(const uint8_t* raw_w, uint8_t* opb,
 // f16 [n / 8][atom a][8 rows][128 B], atom a holding k in [64 a, 64 a + 64) of
 // the CTA's 96 (atom 1 half used), 16-B chunk q of row r at q ^ r.  No
 // transpose: the tensor core reads the weights MN-major.  Unit = (row n, word j
-// of 16 codes = k in [16 j, 16 j + 16)): 768 units, three per weight thread,
-// rows varying fastest so that each 8-thread store phase covers 8 rows.  A
-// word goes out as chunk 2j (its even codes) and chunk 2j + 1 (its odd codes),
-// like the forward's decode; here that permutes the MMA's N columns within
-// every 16, and the epilogue puts them back (dx_column).
+// of 16 codes = k in [16 j, 16 j + 16)): 768 units, three per weight thread.
+// A word goes out as chunk 2j (its even codes) and chunk 2j + 1 (its odd
+// codes), like the forward's decode; here that permutes the MMA's N columns
+// within every 16, and the epilogue puts them back (dx_column).
+// Lanes: rows vary fastest (unit u = tid + 256 i is row u % 128, word
+// u / 128), so each 8-lane store phase is 8 consecutive rows of one word, 8
+// distinct 16-byte bank groups.  The 4-byte loads of 32 consecutive rows (48-B
+// stride) are 4-way bank conflicted; a map with conflict-free loads (8 rows x
+// 4 words per warp instruction) made dX 3% slower.
 constexpr int kDxWordUnits = BK * (BN / 2 / 16);
 static_assert(kDxWordUnits % kWThreads == 0, "equal dX weight share per thread");
 constexpr int kDxWordsPerThread = kDxWordUnits / kWThreads;
 static_assert(kDxWordsPerThread * 8 <= 32, "dX weight units fit the 32 staging registers");
+
+__device__ __forceinline__ void dx_word_unit(int tid, int i, int& n, int& j) {
+  const int u = tid + i * kWThreads;
+  n = u % BK;
+  j = u / BK;
+}
 
 // Accumulator column holding output column e of a 32-column block.
 __host__ __device__ constexpr int dx_column(int e) {
@@ -284,8 +300,8 @@ __device__ __forceinline__ void w_dx_load(const uint8_t* raw_w, int tid, uint32_
                                           uint32_t (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < kDxWordsPerThread; ++i) {
-    const int u = tid + i * kWThreads;
-    const int n = u % BK, j = u / BK;
+    int n, j;
+    dx_word_unit(tid, i, n, j);
     const uint32_t x = *reinterpret_cast<const uint32_t*>(
         raw_w + n * (BN / 4) + 24 * static_cast<int>(rank) + 4 * j);
     const uint32_t e = x & 0x33333333u, o = (x >> 2) & 0x33333333u;
@@ -307,8 +323,9 @@ __device__ __forceinline__ void w_dx_load(const uint8_t* raw_w, int tid, uint32_
 __device__ __forceinline__ void w_dx_store(uint8_t* opb, int tid, const uint32_t (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < kDxWordsPerThread; ++i) {
-    const int u = tid + i * kWThreads;
-    const int n = u % BK, j = u / BK, r = n & 7;
+    int n, j;
+    dx_word_unit(tid, i, n, j);
+    const int r = n & 7;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int q = 2 * j + h;
