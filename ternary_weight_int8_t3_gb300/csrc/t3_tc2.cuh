@@ -198,17 +198,16 @@ __device__ __forceinline__ void s8x4_to_f16_evenodd(uint32_t x, uint32_t& even, 
   odd = hsub2(prmt(y, 0x64646464u, 0x4341u), 0x64806480u);
 }
 
-// The dX converters work in two halves: *_load reads the raw bytes and converts
+// The converters work in two halves: *_load reads the raw bytes and converts
 // them into 32 registers as soon as the raw stage has landed, *_store writes
 // them once the operand slot is free, so that the conversion stays off the
-// path from the MMA's release of a slot to the slot's next use.  The forward
-// converts and stores in one pass (measured faster for its 10-stage tiles).
+// path from the MMA's release of a slot to the slot's next use.
 
 // Activation row -> TMEM: thread (quadrant q, half h) owns lane q*32+lane and
 // reduction elements [64h, 64h+64) of the stage.  The raw tile is [128][128 B]
 // in the 128-byte swizzle.  kEvenOdd: within every 16 reduction elements the
 // even ones come first, then the odd ones -- the order in which the forward's
-// weight decode (decode_w_fwd) emits its codes; both operands of the forward
+// weight decode (w_fwd_load) emits its codes; both operands of the forward
 // use it, so the products and their sum are unchanged.  Otherwise natural order.
 template <bool kEvenOdd>
 __device__ __forceinline__ void act_load(const uint8_t* raw_a, int row, int h, uint32_t (&v)[32]) {
@@ -245,24 +244,45 @@ constexpr int kFwdWordUnits = BNH * (BK / 16);
 static_assert(kFwdWordUnits % kWThreads == 0 && BNH % 4 == 0, "equal forward weight share");
 constexpr int kFwdWordsPerThread = kFwdWordUnits / kWThreads;
 
-__device__ __forceinline__ void decode_w_fwd(const uint8_t* raw_w, uint8_t* opb, int tid) {
-  const int wl = tid & 31, wwarp = tid >> 5;
+__device__ __forceinline__ void fwd_word_unit(int tid, int i, int& row, int& w) {
+  const int wl = tid & 31;
+  const int g = i * (kWThreads / 32) + (tid >> 5);  // group of four rows
+  row = 4 * g + ((wl >> 2) & 1) + 2 * ((wl >> 3) & 1);
+  w = (wl & 3) + 4 * (wl >> 4);
+}
+
+__device__ __forceinline__ void w_fwd_load(const uint8_t* raw_w, int tid, uint32_t (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < kFwdWordsPerThread; ++i) {
-    const int g = i * (kWThreads / 32) + wwarp;  // group of four rows
-    const int row = 4 * g + ((wl >> 2) & 1) + 2 * ((wl >> 3) & 1);
-    const int w = (wl & 3) + 4 * (wl >> 4);
+    int row, w;
+    fwd_word_unit(tid, i, row, w);
     const uint32_t x = *reinterpret_cast<const uint32_t*>(raw_w + row * 32 + 4 * w);
     const uint32_t e = x & 0x33333333u, o = (x >> 2) & 0x33333333u;
     const uint32_t he0 = prmt(tc::kF16HiTable, 0u, e);
     const uint32_t he1 = prmt(tc::kF16HiTable, 0u, e >> 16);
     const uint32_t ho0 = prmt(tc::kF16HiTable, 0u, o);
     const uint32_t ho1 = prmt(tc::kF16HiTable, 0u, o >> 16);
+    v[8 * i + 0] = prmt(he0, 0u, 0x1404u);
+    v[8 * i + 1] = prmt(he0, 0u, 0x3424u);
+    v[8 * i + 2] = prmt(he1, 0u, 0x1404u);
+    v[8 * i + 3] = prmt(he1, 0u, 0x3424u);
+    v[8 * i + 4] = prmt(ho0, 0u, 0x1404u);
+    v[8 * i + 5] = prmt(ho0, 0u, 0x3424u);
+    v[8 * i + 6] = prmt(ho1, 0u, 0x1404u);
+    v[8 * i + 7] = prmt(ho1, 0u, 0x3424u);
+  }
+}
+
+__device__ __forceinline__ void w_fwd_store(uint8_t* opb, int tid, const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < kFwdWordsPerThread; ++i) {
+    int row, w;
+    fwd_word_unit(tid, i, row, w);
     uint8_t* atom = opb + (w >> 2) * Layout<kOpFwd>::opb_atom;
-    sts128(atom + tc::sw128(row, 2 * (w & 3)), prmt(he0, 0u, 0x1404u),
-           prmt(he0, 0u, 0x3424u), prmt(he1, 0u, 0x1404u), prmt(he1, 0u, 0x3424u));
-    sts128(atom + tc::sw128(row, 2 * (w & 3) + 1), prmt(ho0, 0u, 0x1404u),
-           prmt(ho0, 0u, 0x3424u), prmt(ho1, 0u, 0x1404u), prmt(ho1, 0u, 0x3424u));
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      sts128(atom + tc::sw128(row, 2 * (w & 3) + h), v[8 * i + 4 * h], v[8 * i + 4 * h + 1],
+             v[8 * i + 4 * h + 2], v[8 * i + 4 * h + 3]);
   }
 }
 
@@ -409,43 +429,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint8_t* ra = raw + rs * L::raw_stage;
         const uint32_t act_taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kActCol +
                                    os * (BK / 2) + 32 * h;
-        if (OP == kOpFwd) {
-          ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2) &&
-               mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          if (act_warp) {
-            uint32_t v[32];
-            act_load<true>(ra, row, h, v);
-            tmem_st_32x32b_x32(act_taddr, v);
-            tmem_wait_st();
-          } else {
-            decode_w_fwd(ra + RAW_A, opb + os * L::opb_stage, wtid);
-            fence_proxy_async_smem();
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&raw_empty[rs]);
+        // convert as soon as the raw stage is in, release it, and wait for the
+        // operand slot only before storing: the two-slot ring runs latency-bound
+        // on the slot hand-off, which the conversion then stays off
+        ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        uint32_t v[32];
+        if (act_warp)
+          act_load<OP == kOpFwd>(ra, row, h, v);
+        else if (OP == kOpFwd)
+          w_fwd_load(ra + RAW_A, wtid, v);
+        else
+          w_dx_load(ra + RAW_A, wtid, rank, v);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[rs]);
+        ok = mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        if (act_warp) {
+          tmem_st_32x32b_x32(act_taddr, v);
+          tmem_wait_st();
         } else {
-          // dX converts as soon as the raw stage is in, releases it, and waits
-          // for the operand slot only before storing: its 27-stage tiles run
-          // latency-bound on the slot hand-off
-          ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          uint32_t v[32];
-          if (act_warp)
-            act_load<false>(ra, row, h, v);
+          if (OP == kOpFwd)
+            w_fwd_store(opb + os * L::opb_stage, wtid, v);
           else
-            w_dx_load(ra + RAW_A, wtid, rank, v);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&raw_empty[rs]);
-          ok = mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          if (act_warp) {
-            tmem_st_32x32b_x32(act_taddr, v);
-            tmem_wait_st();
-          } else {
             w_dx_store(opb + os * L::opb_stage, wtid, v);
-            fence_proxy_async_smem();
-          }
+          fence_proxy_async_smem();
         }
         tc_fence_before();
         __syncwarp();
