@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pack", action="store_true",
+                    help="skip the device-packer sweep (HBM-bound, reported beside the step)")
     ap.add_argument("--no-small-m", action="store_true",
                     help="skip the small-M forward sweep (for launch-list captures)")
     ap.add_argument("--small-m-only", metavar="M,N,K", default=None,
@@ -227,6 +229,44 @@ def bench_small_m(t3, torch, dev, stream, hbm_gbs, reps=30, configs=None):
                     "GBps": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 3),
                     "TOPS": round(2 * m * n * k / (us * 1e-6) / 1e12, 2), "timing": mode})
         del wps
+    return out
+
+
+PACK_SHAPES = [(1280, 3456), (8192, 8192)]
+
+
+def bench_device_pack(t3, torch, dev, stream, hbm_gbs, reps=20):
+    """Device packer sweep: bytes moved (w in, Wp out) per call over its device
+    time.  Enough distinct copies of w rotate through the calls that no copy is
+    still in the 129 MB L2; the calls are replayed from a CUDA graph."""
+    out = []
+    for (k, n) in PACK_SHAPES:
+        g = t3_synth.rng(4242 + k + n)
+        w = t3_synth.ternary(g, (k, n))
+        copies = max(2, -(-2 * 129 * 2**20 // w.nbytes))
+        w_d = torch.from_numpy(w).to(dev)
+        ws = [w_d.clone() for _ in range(copies)]
+        wp = torch.empty((n, (k + 3) // 4), dtype=torch.uint8, device=dev)
+        for i in range(3):
+            t3.t3_pack_ternary_device(ws[i % copies], wp, stream=stream)
+        torch.cuda.synchronize(dev)
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_):
+            for i in range(reps):
+                t3.t3_pack_ternary_device(ws[i % copies], wp)
+        g_.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g_.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        nbytes = w.nbytes + wp.numel()
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out.append({"K": k, "N": n, "us_per_call": round(us, 3), "bytes": nbytes,
+                    "GBps": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 3), "timing": "graph"})
+        del ws
     return out
 
 
@@ -459,6 +499,8 @@ def main():
         "clocks": clocks.summary(),
     }
     hbm = peaks.get("hbm_gbs", 6800.0) if peak_src == "measured" else 6800.0
+    if not args.no_pack:
+        line["device_pack"] = {"hbm_peak_GBps": hbm, "calls": bench_device_pack(t3, torch, dev, stream, hbm)}
     if not args.no_small_m:
         line["small_m"] = {"hbm_peak_GBps": hbm, "calls": bench_small_m(t3, torch, dev, stream, hbm)}
     if world == 1 and not args.no_cpu_baseline:

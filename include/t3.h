@@ -74,6 +74,19 @@ typedef enum {
 int t3_pack_ternary(const int8_t* w, uint8_t* wp, int64_t K, int64_t N);
 
 /*
+ * t3_pack_ternary_device -- the same packing as t3_pack_ternary, on the device.
+ *   w   DEVICE int8 [K][N]; wp DEVICE uint8 [N][ceil(K/4)], written in full
+ *       (pad codes 0).  Both are owned by the caller.
+ * Asynchronous on `stream`.  A value outside {-1, 0, +1} packs as code 0 and
+ * records (9 << 8) | 6 in the device error word: t3_last_device_error then
+ * returns T3_EVALUE.  Returns T3_EINVAL, without launching, for negative
+ * sizes, null pointers (with K, N > 0) or sizes above 2^31 - 1; K or N = 0 is
+ * a no-op.  Training changes W every step: this keeps the packing on the GPU.
+ */
+int t3_pack_ternary_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N,
+                           t3_stream_t stream);
+
+/*
  * t3_gemm_fwd -- [fwd]: C[m][n] = sum_{k<K} A[m][k] * W[k][n].
  *   A [M][K], Wp [N][ceil(K/4)], C [M][N] (layouts above), device pointers.
  * Exact for every input when K <= 16777215 (|A W| <= 128 K fits int32);
@@ -116,10 +129,12 @@ const char* t3_status_string(int status);
  * stop early, leaving its output incomplete, and records a code in a
  * per-device error word instead of hanging the GPU.  This call synchronizes
  * `stream`, returns T3_ETIMEOUT if the word is set (T3_OK otherwise) and
- * clears it.  *detail, when not NULL, receives the recorded code (0 if none):
- * bits 0-7 the role that gave up (1 producer, 2 converter, 3 MMA issuer,
- * 4 epilogue, 5 pair forwarder), bits 8-15 the kernel (1 fwd, 2 dX, 3 dW on
- * one CTA per tile; 4 small-M fwd; 5 fwd, 6 dX, 7 dW on CTA pairs).
+ * clears it; T3_EVALUE instead when the code is the device packer's invalid
+ * value.  *detail, when not NULL, receives the recorded code (0 if none):
+ * bits 0-7 the role (1 producer, 2 converter, 3 MMA issuer, 4 epilogue,
+ * 5 pair forwarder gave up; 6 an input value was invalid), bits 8-15 the
+ * kernel (1 fwd, 2 dX, 3 dW on one CTA per tile; 4 small-M fwd; 5 fwd, 6 dX,
+ * 7 dW on CTA pairs; 9 the device packer).
  */
 int t3_last_device_error(t3_stream_t stream, int32_t* detail);
 

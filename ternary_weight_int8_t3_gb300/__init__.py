@@ -7,6 +7,7 @@ is no fallback: if the library is missing or cannot load, every call raises.
 
 Function names follow the C ABI:
   t3_pack_ternary(w)                       host packer, w int8 [K][N]
+  t3_pack_ternary_device(w, wp=None)       the same on the GPU (w a CUDA tensor)
   t3_gemm_fwd(A, Wp, K=None, C=None)       C  = A . W        (int32 [M][N])
   t3_gemm_bwd_dx(dY, Wp, K, dX=None)       dX = dY . W^T     (int32 [M][K])
   t3_gemm_bwd_dw(A, dY, dW=None)           dW = A^T . dY     (int32 [K][N])
@@ -59,6 +60,8 @@ def load():
             f.argtypes = [p, p, p, i64, i64, i64, p]
             f.restype = ctypes.c_int
         lib.t3_pack_ternary.restype = ctypes.c_int
+        lib.t3_pack_ternary_device.argtypes = [p, p, i64, i64, p]
+        lib.t3_pack_ternary_device.restype = ctypes.c_int
         lib.t3_status_string.argtypes = [ctypes.c_int]
         lib.t3_status_string.restype = ctypes.c_char_p
         lib.t3_last_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
@@ -124,6 +127,24 @@ def _stream(t, stream):
     torch = _torch()
     s = stream if stream is not None else torch.cuda.current_stream(t.device)
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def t3_pack_ternary_device(w, wp=None, stream=None):
+    """Packs ternary w (CUDA int8 tensor [K][N]) into Wp (CUDA uint8
+    [N][ceil(K/4)]) on the GPU, asynchronously on `stream`.  A value outside
+    {-1, 0, +1} packs as 0 and is reported by t3_last_device_error."""
+    torch = _torch()
+    if not isinstance(w, torch.Tensor) or w.dim() != 2:
+        raise TypeError("w must be a 2-D CUDA int8 tensor [K][N]")
+    K, N = w.shape
+    if wp is None:
+        wp = torch.empty((N, (K + 3) // 4), dtype=torch.uint8, device=w.device)
+    if tuple(wp.shape) != (N, (K + 3) // 4):
+        raise ValueError(f"wp must be [{N}][{(K + 3) // 4}], got {tuple(wp.shape)}")
+    rc = load().t3_pack_ternary_device(_dev_ptr(w, torch.int8, "w"), _dev_ptr(wp, torch.uint8, "wp"),
+                                       K, N, _stream(w, stream))
+    _check(rc, "t3_pack_ternary_device")
+    return wp
 
 
 def t3_gemm_fwd(A, Wp, K: int | None = None, C=None, stream=None):

@@ -313,6 +313,17 @@ int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, in
                        tc::kChunkKbInt8, stream);
 }
 
+int t3_pack_ternary_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N,
+                           t3_stream_t stream) {
+  if (K < 0 || N < 0 || K > kMaxDim || N > kMaxDim) return T3_EINVAL;
+  if (K == 0 || N == 0) return T3_OK;
+  if (!w || !wp) return T3_EINVAL;
+  const DeviceInfo* dev = nullptr;
+  const int st = device_info(&dev);
+  if (st != T3_OK) return st;
+  return launch_pack_device(w, wp, K, N, dev->sms, dev->err_word, stream);
+}
+
 const char* t3_status_string(int status) {
   switch (status) {
     case T3_OK: return "T3_OK: success";
@@ -341,7 +352,8 @@ int t3_last_device_error(t3_stream_t stream, int32_t* detail) {
       return T3_ECUDA;
   }
   if (detail) *detail = value;
-  return value ? T3_ETIMEOUT : T3_OK;
+  if (value == 0) return T3_OK;
+  return (value & 0xFF) == 6 ? T3_EVALUE : T3_ETIMEOUT;  // role 6: an invalid input value
 }
 
 int t3_version(void) { return 100; }

@@ -41,6 +41,11 @@ int launch_zero_pdl(int32_t* out, int64_t n, int sms, cudaStream_t s);
 int launch_dw2(const dw2::Params& p, const CUtensorMap& ma, const CUtensorMap& mdy,
                const CUtensorMap& mo, int grid, cudaStream_t s);
 
+// Device packer: int8 w [K][N] -> Wp [N][ceil(K/4)] on `s`; a value outside
+// {-1, 0, +1} packs as 0 and records (9 << 8) | 6 in *err.
+int launch_pack_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N, int sms, int* err,
+                       cudaStream_t s);
+
 // Small-M forward (M <= 32): zeroes C on `s`, then accumulates into it.
 int launch_skinny_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,
                       int64_t K, int sms, int* err, cudaStream_t s);
