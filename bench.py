@@ -235,6 +235,41 @@ def bench_small_m(t3, torch, dev, stream, hbm_gbs, reps=30, configs=None):
 PACK_SHAPES = [(1280, 3456), (8192, 8192)]
 
 
+def bench_scaled(t3, torch, dev, stream, A_d, wp_d, dY_d, K, reps=10):
+    """The layer step's three products with scaled float output (row scales
+    per output row, column scales per output column): fwd and dX scale in the
+    pair pipeline's epilogue, dW converts its exact int32 result in place."""
+    M, N = A_d.shape[0], wp_d.shape[0]
+    g = torch.Generator(device="cpu").manual_seed(99)
+    def sc(n):
+        return (torch.randn(n, generator=g) * 0.01).to(dev)
+    rs_m, cs_n, cs_k, rs_k = sc(M), sc(N), sc(K), sc(K)
+    C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    dX = torch.empty((M, K), dtype=torch.float32, device=dev)
+    dW = torch.empty((K, N), dtype=torch.float32, device=dev)
+    calls = {
+        "fwd": lambda: t3.t3_gemm_fwd_scaled(A_d, wp_d, K, rs_m, cs_n, t3.T3_OUT_F32, C=C, stream=stream),
+        "dx": lambda: t3.t3_gemm_bwd_dx_scaled(dY_d, wp_d, K, rs_m, cs_k, t3.T3_OUT_F32, dX=dX,
+                                               stream=stream),
+        "dw": lambda: t3.t3_gemm_bwd_dw_scaled(A_d, dY_d, rs_k, cs_n, t3.T3_OUT_F32, dW=dW,
+                                               stream=stream),
+    }
+    out = {}
+    for name, call in calls.items():
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / reps
+        out[name] = {"us": round(ms * 1e3, 1), "TOPS": round(OPS_PER_PRODUCT / (ms * 1e-3) / 1e12, 1)}
+    return out
+
+
 def bench_device_pack(t3, torch, dev, stream, hbm_gbs, reps=20):
     """Device packer sweep: bytes moved (w in, Wp out) per call over its device
     time.  Enough distinct copies of w rotate through the calls that no copy is
@@ -499,6 +534,7 @@ def main():
         "clocks": clocks.summary(),
     }
     hbm = peaks.get("hbm_gbs", 6800.0) if peak_src == "measured" else 6800.0
+    line["scaled_f32"] = bench_scaled(t3, torch, dev, stream, A_d, wp_d, dY_d, K)
     if not args.no_pack:
         line["device_pack"] = {"hbm_peak_GBps": hbm, "calls": bench_device_pack(t3, torch, dev, stream, hbm)}
     if not args.no_small_m:

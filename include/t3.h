@@ -120,6 +120,57 @@ int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, 
 int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N,
                    int64_t K, t3_stream_t stream);
 
+/*
+ * Scaled outputs -- the step after the products in "spec(igla): hslm_bwd_ptx
+ * -- HSLM backward dX and dW as int8 tensor-core PTX written by t27": the
+ * host rescales the integer results (dX by a scale per row; dW by scales per
+ * column of X and of dY, i.e. per row and per column of dW), and the products
+ * also have "+=" forms.  For an exact int32 result x[r][c]:
+ *   y = ((float)x * row_scale[r]) * col_scale[c]
+ * with each conversion and product rounded to the nearest float (ties to
+ * even); a NULL scale vector stands for ones.  The output kind decides what
+ * is written: T3_OUT_F32 stores y (float), T3_OUT_BF16 stores y rounded to
+ * bf16 (nearest, ties to even), T3_OUT_F32_ADD sets out = out + y (float, one
+ * rounding).  Scale vectors are device float arrays, owned by the caller.
+ */
+enum { T3_OUT_F32 = 0, T3_OUT_BF16 = 1, T3_OUT_F32_ADD = 2 };
+
+/*
+ * t3_dequant_i32 -- out[r][c] from x [rows][cols] (DEVICE int32) as above;
+ *   out DEVICE [rows][cols] float or bf16; row_scale [rows], col_scale [cols].
+ * x and out may be the same buffer for T3_OUT_F32 only (else T3_EINVAL).
+ * Asynchronous on `stream`; rows or cols = 0 is a no-op.
+ */
+int t3_dequant_i32(const int32_t* x, void* out, int64_t rows, int64_t cols,
+                   const float* row_scale, const float* col_scale, int out_kind,
+                   t3_stream_t stream);
+
+/*
+ * t3_gemm_fwd_scaled, t3_gemm_bwd_dx_scaled, t3_gemm_bwd_dw_scaled -- the
+ * products of t3_gemm_fwd / t3_gemm_bwd_dx / t3_gemm_bwd_dw with the scaled
+ * output above, same operands, sizes, validation and overflow rules:
+ *   fwd: C [M][N],  row_scale [M], col_scale [N];
+ *   dX:  dX [M][K], row_scale [M], col_scale [K];
+ *   dW:  dW [K][N], row_scale [K] (X's column scales), col_scale [N] (dY's).
+ * The forward (M > 32) and dX apply the scales in the epilogue of their
+ * pair pipeline when the reduction is at most 65536 long and the output rows
+ * are 16-byte aligned; otherwise, and always for dW, they compute the exact
+ * int32 product first and then run t3_dequant_i32.  That product goes to
+ * `workspace` (DEVICE int32 with the output's rows x cols, caller-owned) or,
+ * for T3_OUT_F32 when `workspace` is NULL, into the output buffer, converted
+ * in place; T3_OUT_BF16 and T3_OUT_F32_ADD return T3_EINVAL there without a
+ * workspace.  The result is the same on every path.
+ */
+int t3_gemm_fwd_scaled(const int8_t* A, const uint8_t* Wp, void* C, int64_t M, int64_t N,
+                       int64_t K, const float* row_scale, const float* col_scale, int out_kind,
+                       int32_t* workspace, t3_stream_t stream);
+int t3_gemm_bwd_dx_scaled(const int8_t* dY, const uint8_t* Wp, void* dX, int64_t M, int64_t N,
+                          int64_t K, const float* row_scale, const float* col_scale, int out_kind,
+                          int32_t* workspace, t3_stream_t stream);
+int t3_gemm_bwd_dw_scaled(const int8_t* A, const int8_t* dY, void* dW, int64_t M, int64_t N,
+                          int64_t K, const float* row_scale, const float* col_scale, int out_kind,
+                          int32_t* workspace, t3_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* t3_status_string(int status);
 

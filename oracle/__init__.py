@@ -13,6 +13,10 @@ arrays.  What each function follows on the pages is cited in the C source:
   2-bit decode formula, the row reference.
 * "spec(igla): hslm_bwd_ptx -- HSLM backward dX and dW as int8 tensor-core PTX
   written by t27", kernel 1 (dX) and kernel 2 (dW).
+
+The scaled outputs (``dequant``, ``bf16_bits``) are written here in numpy
+float32 arithmetic, which rounds every conversion, product and sum to the
+nearest float (ties to even), as their definition asks.
 """
 from __future__ import annotations
 
@@ -184,6 +188,41 @@ def dw(A, dY, rows=None) -> np.ndarray:
                                 None if r is None else _ptr(r), nr)
     _check(rc, "oracle_dw")
     return dW
+
+
+OUT_F32, OUT_BF16, OUT_F32_ADD = 0, 1, 2
+
+
+def bf16_bits(y) -> np.ndarray:
+    """float32 values -> bf16 bit patterns (uint16), rounded to nearest, ties
+    to even: add half an ulp of the kept 16 bits (0x7FFF, plus the kept
+    lowest bit for ties) and keep the high half.  Finite inputs."""
+    u = np.ascontiguousarray(y, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def dequant(x, row_scale=None, col_scale=None, kind: int = OUT_F32, out=None) -> np.ndarray:
+    """The scaled output of an exact int32 result x [rows][cols]: the step after
+    the products in "spec(igla): hslm_bwd_ptx -- HSLM backward dX and dW as
+    int8 tensor-core PTX written by t27", where the host rescales the integer
+    results (dX per row, dW per column of X and of dY) and the products have
+    "+=" forms.  y = ((float)x * row_scale[r]) * col_scale[c], every step a
+    float32 operation; None scales are ones.  Returns y (OUT_F32), its bf16
+    bit patterns (OUT_BF16), or out + y (OUT_F32_ADD, `out` the old float32
+    values)."""
+    x = np.asarray(x, dtype=np.int32)
+    rows, cols = x.shape
+    rs = np.ones(rows, np.float32) if row_scale is None else np.asarray(row_scale, np.float32)
+    cs = np.ones(cols, np.float32) if col_scale is None else np.asarray(col_scale, np.float32)
+    y = x.astype(np.float32) * rs[:, None]
+    y = y * cs[None, :]
+    if kind == OUT_F32:
+        return y
+    if kind == OUT_BF16:
+        return bf16_bits(y)
+    if kind == OUT_F32_ADD:
+        return np.asarray(out, dtype=np.float32) + y
+    raise ValueError(f"unknown output kind {kind}")
 
 
 def num_threads() -> int:

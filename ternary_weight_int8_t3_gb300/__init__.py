@@ -11,6 +11,9 @@ Function names follow the C ABI:
   t3_gemm_fwd(A, Wp, K=None, C=None)       C  = A . W        (int32 [M][N])
   t3_gemm_bwd_dx(dY, Wp, K, dX=None)       dX = dY . W^T     (int32 [M][K])
   t3_gemm_bwd_dw(A, dY, dW=None)           dW = A^T . dY     (int32 [K][N])
+  t3_dequant_i32(x, kind, row_scale, col_scale, out=None)   scaled float/bf16 output
+  t3_gemm_fwd_scaled / t3_gemm_bwd_dx_scaled / t3_gemm_bwd_dw_scaled
+                                           the products with that output
 """
 from __future__ import annotations
 
@@ -26,6 +29,7 @@ LIB_PATH = os.path.join(_PKG, "libt3.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "t3.h")
 
 T3_OK, T3_EINVAL, T3_EVALUE, T3_EOVERFLOW, T3_ECUDA, T3_ETIMEOUT, T3_EDEVICE = 0, -1, -2, -3, -4, -5, -6
+T3_OUT_F32, T3_OUT_BF16, T3_OUT_F32_ADD = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +66,12 @@ def load():
         lib.t3_pack_ternary.restype = ctypes.c_int
         lib.t3_pack_ternary_device.argtypes = [p, p, i64, i64, p]
         lib.t3_pack_ternary_device.restype = ctypes.c_int
+        lib.t3_dequant_i32.argtypes = [p, p, i64, i64, p, p, ctypes.c_int, p]
+        lib.t3_dequant_i32.restype = ctypes.c_int
+        for name in ("t3_gemm_fwd_scaled", "t3_gemm_bwd_dx_scaled", "t3_gemm_bwd_dw_scaled"):
+            f = getattr(lib, name)
+            f.argtypes = [p, p, p, i64, i64, i64, p, p, ctypes.c_int, p, p]
+            f.restype = ctypes.c_int
         lib.t3_status_string.argtypes = [ctypes.c_int]
         lib.t3_status_string.restype = ctypes.c_char_p
         lib.t3_last_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
@@ -206,6 +216,109 @@ def t3_gemm_bwd_dw(A, dY, dW=None, stream=None):
     with torch.cuda.device(A.device):
         rc = load().t3_gemm_bwd_dw(*args, M, N, K, _stream(A, stream))
     _check(rc, "t3_gemm_bwd_dw")
+    return dW
+
+
+# ------------------------------------------------------------ scaled outputs
+
+def _scaled_out(out, kind, rows, cols, device, name):
+    torch = _torch()
+    dtype = torch.bfloat16 if kind == T3_OUT_BF16 else torch.float32
+    if kind not in (T3_OUT_F32, T3_OUT_BF16, T3_OUT_F32_ADD):
+        raise ValueError(f"unknown output kind {kind}")
+    if out is None:
+        if kind == T3_OUT_F32_ADD:
+            raise ValueError(f"{name}: the += kind needs the existing output")
+        out = torch.empty((rows, cols), dtype=dtype, device=device)
+    if tuple(out.shape) != (rows, cols):
+        raise ValueError(f"{name} must be [{rows}][{cols}]")
+    return out, _dev_ptr(out, dtype, name)
+
+
+def _scale_ptr(v, n, name):
+    if v is None:
+        return ctypes.c_void_p(0)
+    if v.dim() != 1 or v.shape[0] != n:
+        raise ValueError(f"{name} must have {n} entries")
+    return _dev_ptr(v, _torch().float32, name)
+
+
+def _ws_ptr(ws, rows, cols):
+    if ws is None:
+        return ctypes.c_void_p(0)
+    if tuple(ws.shape) != (rows, cols):
+        raise ValueError(f"workspace must be [{rows}][{cols}]")
+    return _dev_ptr(ws, _torch().int32, "workspace")
+
+
+def t3_dequant_i32(x, kind=T3_OUT_F32, row_scale=None, col_scale=None, out=None, stream=None):
+    """out = ((float)x * row_scale[r]) * col_scale[c] as float (T3_OUT_F32),
+    bf16 (T3_OUT_BF16) or added to `out` (T3_OUT_F32_ADD).  x int32 [R][C]."""
+    torch = _torch()
+    rows, cols = x.shape
+    out, po = _scaled_out(out, kind, rows, cols, x.device, "out")
+    args = (_dev_ptr(x, torch.int32, "x"), po, rows, cols, _scale_ptr(row_scale, rows, "row_scale"),
+            _scale_ptr(col_scale, cols, "col_scale"), kind, _stream(x, stream))
+    with torch.cuda.device(x.device):
+        rc = load().t3_dequant_i32(*args)
+    _check(rc, "t3_dequant_i32")
+    return out
+
+
+def t3_gemm_fwd_scaled(A, Wp, K=None, row_scale=None, col_scale=None, kind=T3_OUT_F32, C=None,
+                       workspace=None, stream=None):
+    """C (scaled, float or bf16 [M][N]) of A . W; row_scale [M], col_scale [N]."""
+    torch = _torch()
+    M, Ka = A.shape
+    K = Ka if K is None else K
+    if Ka != K:
+        raise ValueError("A must be [M][K]")
+    N = Wp.shape[0]
+    if Wp.dim() != 2 or Wp.shape[1] != (K + 3) // 4:
+        raise ValueError("Wp must be [N][ceil(K/4)]")
+    C, pc = _scaled_out(C, kind, M, N, A.device, "C")
+    args = (_dev_ptr(A, torch.int8, "A"), _dev_ptr(Wp, torch.uint8, "Wp"), pc, M, N, K,
+            _scale_ptr(row_scale, M, "row_scale"), _scale_ptr(col_scale, N, "col_scale"), kind,
+            _ws_ptr(workspace, M, N), _stream(A, stream))
+    with torch.cuda.device(A.device):
+        rc = load().t3_gemm_fwd_scaled(*args)
+    _check(rc, "t3_gemm_fwd_scaled")
+    return C
+
+
+def t3_gemm_bwd_dx_scaled(dY, Wp, K: int, row_scale=None, col_scale=None, kind=T3_OUT_F32,
+                          dX=None, workspace=None, stream=None):
+    """dX (scaled, float or bf16 [M][K]) of dY . W^T; row_scale [M], col_scale [K]."""
+    torch = _torch()
+    M, N = dY.shape
+    if Wp.dim() != 2 or tuple(Wp.shape) != (N, (K + 3) // 4):
+        raise ValueError("Wp must be [N][ceil(K/4)]")
+    dX, px = _scaled_out(dX, kind, M, K, dY.device, "dX")
+    args = (_dev_ptr(dY, torch.int8, "dY"), _dev_ptr(Wp, torch.uint8, "Wp"), px, M, N, K,
+            _scale_ptr(row_scale, M, "row_scale"), _scale_ptr(col_scale, K, "col_scale"), kind,
+            _ws_ptr(workspace, M, K), _stream(dY, stream))
+    with torch.cuda.device(dY.device):
+        rc = load().t3_gemm_bwd_dx_scaled(*args)
+    _check(rc, "t3_gemm_bwd_dx_scaled")
+    return dX
+
+
+def t3_gemm_bwd_dw_scaled(A, dY, row_scale=None, col_scale=None, kind=T3_OUT_F32, dW=None,
+                          workspace=None, stream=None):
+    """dW (scaled, float or bf16 [K][N]) of A^T . dY; row_scale [K] (A's column
+    scales), col_scale [N] (dY's column scales)."""
+    torch = _torch()
+    M, K = A.shape
+    if dY.shape[0] != M:
+        raise ValueError("A and dY must have the same number of rows")
+    N = dY.shape[1]
+    dW, pw = _scaled_out(dW, kind, K, N, A.device, "dW")
+    args = (_dev_ptr(A, torch.int8, "A"), _dev_ptr(dY, torch.int8, "dY"), pw, M, N, K,
+            _scale_ptr(row_scale, K, "row_scale"), _scale_ptr(col_scale, N, "col_scale"), kind,
+            _ws_ptr(workspace, K, N), _stream(A, stream))
+    with torch.cuda.device(A.device):
+        rc = load().t3_gemm_bwd_dw_scaled(*args)
+    _check(rc, "t3_gemm_bwd_dw_scaled")
     return dW
 
 

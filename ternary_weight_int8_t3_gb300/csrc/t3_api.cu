@@ -68,6 +68,29 @@ bool make_i32_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_
   return r == CUDA_SUCCESS;
 }
 
+// Output tensor map of the pair pipeline for output kind `kind` (tc2::kOutI32
+// or a T3_OUT_* kind): boxes of 32 columns x 128 rows; int32 and float rows
+// in the 128-byte swizzle, bf16 rows (64 bytes) unswizzled.
+bool make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int kind) {
+  if (kind == tc2::kOutI32) return make_i32_map_tiled(map, base, rows, cols, 128, 32, true);
+  std::memset(map, 0, sizeof(*map));
+  const int64_t esize = (kind == T3_OUT_BF16) ? 2 : 4;
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (cols * esize) % 16 != 0) return false;
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esize)};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map,
+                  kind == T3_OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  kind == T3_OUT_BF16 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) std::memset(map, 0, sizeof(*map));
+  return r == CUDA_SUCCESS;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -154,10 +177,13 @@ int run_tc(const uint8_t* a_src, int64_t a_rows, int64_t a_cols, const uint8_t* 
 // The CTA-pair pipeline for the forward (OP = kOpFwd: act = A [M][K], weights
 // packed along K) or dX (act = dY [M][N], reduction N).  Returns T3_EINVAL
 // without launching when an operand cannot be a TMA source or the output
-// cannot take bulk stores; the caller then uses the single-CTA pipeline.
+// cannot take bulk stores; the caller then uses the single-CTA pipeline (or,
+// for a scaled output kind, the exact int32 product and t3_dequant_i32).  A
+// scaled kind needs the reduction in one exact chunk.
 template <int OP>
-int run_tc2(const int8_t* act, const uint8_t* Wp, int32_t* out, int64_t M, int64_t N, int64_t K,
-            cudaStream_t stream) {
+int run_tc2(const int8_t* act, const uint8_t* Wp, void* out, int64_t M, int64_t N, int64_t K,
+            cudaStream_t stream, int out_kind = tc2::kOutI32, const float* row_scale = nullptr,
+            const float* col_scale = nullptr) {
   const DeviceInfo* dev = nullptr;
   int st = device_info(&dev);
   if (st != T3_OK) return st;
@@ -170,7 +196,8 @@ int run_tc2(const int8_t* act, const uint8_t* Wp, int32_t* out, int64_t M, int64
                         ? make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BNH, tc2::BK / 4)
                         : make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BK, tc2::BN / 4);
   if (!w_ok) return T3_EINVAL;
-  if (!make_i32_map_tiled(&mo, out, M, out_cols, 128, 32, true)) return T3_EINVAL;
+  if (!make_out_map(&mo, out, M, out_cols, out_kind)) return T3_EINVAL;
+  if (out_kind != tc2::kOutI32 && ceil_div(act_cols, tc2::BK) > tc2::kChunkStages) return T3_EINVAL;
   tc2::Params p{};
   p.M = M;
   p.N = N;
@@ -182,8 +209,11 @@ int run_tc2(const int8_t* act, const uint8_t* Wp, int32_t* out, int64_t M, int64
   if (tiles_r * tiles_c > kMaxDim) return T3_EINVAL;
   p.tiles_r = static_cast<int>(tiles_r);
   p.tiles_c = static_cast<int>(tiles_c);
-  p.out = out;
+  p.out = static_cast<int32_t*>(out);
   p.use_tma_out = 1;
+  p.out_kind = out_kind;
+  p.row_scale = row_scale;
+  p.col_scale = col_scale;
   p.err = dev->err_word;
   const int64_t pairs = std::min<int64_t>(tiles_r * tiles_c, dev->sms / 2);
   const int grid = static_cast<int>(2 * pairs);
@@ -219,6 +249,27 @@ int run_dw2(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N
   st = launch_zero_pdl(dW, K * N, dev->sms, stream);
   if (st != T3_OK) return st;
   return launch_dw2(p, ma, mdy, mo, static_cast<int>(2 * pairs), stream);
+}
+
+bool valid_out_kind(int kind) {
+  return kind == T3_OUT_F32 || kind == T3_OUT_BF16 || kind == T3_OUT_F32_ADD;
+}
+
+// The scaled products where the pair pipeline cannot scale in its epilogue:
+// the exact int32 product into `workspace` (or, for float output without
+// accumulation, into the output buffer itself, converted in place), then
+// the dequantization.  bf16 and "+=" outputs need the workspace.
+template <class Product>
+int scaled_two_pass(Product product, void* out, int64_t rows, int64_t cols, const float* row_scale,
+                    const float* col_scale, int kind, int32_t* workspace, cudaStream_t stream) {
+  int32_t* x = workspace ? workspace : (kind == T3_OUT_F32 ? static_cast<int32_t*>(out) : nullptr);
+  if (!x) return T3_EINVAL;
+  int st = product(x);
+  if (st != T3_OK) return st;
+  const DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != T3_OK) return st;
+  return launch_dequant(x, out, rows, cols, row_scale, col_scale, kind, dev->sms, stream);
 }
 
 bool bad_dims(int64_t M, int64_t N, int64_t K) {
@@ -322,6 +373,66 @@ int t3_pack_ternary_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N,
   const int st = device_info(&dev);
   if (st != T3_OK) return st;
   return launch_pack_device(w, wp, K, N, dev->sms, dev->err_word, stream);
+}
+
+int t3_dequant_i32(const int32_t* x, void* out, int64_t rows, int64_t cols,
+                   const float* row_scale, const float* col_scale, int out_kind,
+                   t3_stream_t stream) {
+  if (rows < 0 || cols < 0 || !valid_out_kind(out_kind)) return T3_EINVAL;
+  if (rows == 0 || cols == 0) return T3_OK;
+  if (!x || !out) return T3_EINVAL;
+  if (out_kind != T3_OUT_F32 && static_cast<const void*>(x) == out) return T3_EINVAL;
+  const DeviceInfo* dev = nullptr;
+  const int st = device_info(&dev);
+  if (st != T3_OK) return st;
+  return launch_dequant(x, out, rows, cols, row_scale, col_scale, out_kind, dev->sms, stream);
+}
+
+int t3_gemm_fwd_scaled(const int8_t* A, const uint8_t* Wp, void* C, int64_t M, int64_t N,
+                       int64_t K, const float* row_scale, const float* col_scale, int out_kind,
+                       int32_t* workspace, t3_stream_t stream) {
+  if (bad_dims(M, N, K) || !valid_out_kind(out_kind)) return T3_EINVAL;
+  if (M == 0 || N == 0) return T3_OK;
+  if (!C) return T3_EINVAL;
+  if (K > 0 && (!A || !Wp)) return T3_EINVAL;
+  if (K > kMaxTernaryReduction) return T3_EOVERFLOW;
+  if (M > kSmallM && K > 0) {
+    const int st = run_tc2<kOpFwd>(A, Wp, C, M, N, K, stream, out_kind, row_scale, col_scale);
+    if (st != T3_EINVAL) return st;
+  }
+  return scaled_two_pass(
+      [&](int32_t* x) { return t3_gemm_fwd(A, Wp, x, M, N, K, stream); }, C, M, N, row_scale,
+      col_scale, out_kind, workspace, stream);
+}
+
+int t3_gemm_bwd_dx_scaled(const int8_t* dY, const uint8_t* Wp, void* dX, int64_t M, int64_t N,
+                          int64_t K, const float* row_scale, const float* col_scale, int out_kind,
+                          int32_t* workspace, t3_stream_t stream) {
+  if (bad_dims(M, N, K) || !valid_out_kind(out_kind)) return T3_EINVAL;
+  if (M == 0 || K == 0) return T3_OK;
+  if (!dX) return T3_EINVAL;
+  if (N > 0 && (!dY || !Wp)) return T3_EINVAL;
+  if (N > kMaxTernaryReduction) return T3_EOVERFLOW;
+  if (N > 0) {
+    const int st = run_tc2<kOpDx>(dY, Wp, dX, M, N, K, stream, out_kind, row_scale, col_scale);
+    if (st != T3_EINVAL) return st;
+  }
+  return scaled_two_pass(
+      [&](int32_t* x) { return t3_gemm_bwd_dx(dY, Wp, x, M, N, K, stream); }, dX, M, K,
+      row_scale, col_scale, out_kind, workspace, stream);
+}
+
+int t3_gemm_bwd_dw_scaled(const int8_t* A, const int8_t* dY, void* dW, int64_t M, int64_t N,
+                          int64_t K, const float* row_scale, const float* col_scale, int out_kind,
+                          int32_t* workspace, t3_stream_t stream) {
+  if (bad_dims(M, N, K) || !valid_out_kind(out_kind)) return T3_EINVAL;
+  if (K == 0 || N == 0) return T3_OK;
+  if (!dW) return T3_EINVAL;
+  if (M > 0 && (!A || !dY)) return T3_EINVAL;
+  if (M > kMaxInt8Reduction) return T3_EOVERFLOW;
+  return scaled_two_pass(
+      [&](int32_t* x) { return t3_gemm_bwd_dw(A, dY, x, M, N, K, stream); }, dW, K, N, row_scale,
+      col_scale, out_kind, workspace, stream);
 }
 
 const char* t3_status_string(int status) {

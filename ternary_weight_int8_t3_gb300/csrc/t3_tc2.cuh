@@ -30,7 +30,11 @@
 // per converter warp: a cluster-scope release costs the issuing thread
 // hundreds of nanoseconds), warps 18-21 are the epilogue.
 #pragma once
+#include <cuda_bf16.h>
+
 #include <cstdint>
+
+#include "t3.h"
 #include "t3_tc_gemm.cuh"
 
 namespace t3 {
@@ -73,11 +77,16 @@ template <int OP> struct Layout {
   static constexpr int off_opb = 0;
   static constexpr int off_raw = off_opb + OP_STAGES * opb_stage;
   static constexpr int off_out = off_raw + RAW_STAGES * raw_stage;
-  static constexpr int off_bar = off_out + 2 * stage_out;
+  static constexpr int off_cs = off_out + 2 * stage_out;  // a tile's column scales
+  static constexpr int off_bar = off_cs + BN * 4;
   static constexpr int n_bars = 2 * RAW_STAGES + 3 * OP_STAGES + 2 * ACC_BUFS + 1;
   static constexpr int off_misc = off_bar + 8 * n_bars;
   static constexpr int smem_alloc = off_misc + 16 + 1024;
 };
+
+// Output kind of the pair pipeline: the exact int32 product, or (one exact
+// chunk only, bulk stores only) the scaled forms of t3_dequant_i32.
+constexpr int kOutI32 = -1;
 
 struct Params {
   int64_t M, N, K;        // the product's M, N, K
@@ -86,8 +95,40 @@ struct Params {
   int tiles_r, tiles_c;
   int32_t* out;           // used when the output cannot take bulk stores
   int use_tma_out;
+  int out_kind;           // kOutI32, T3_OUT_F32, T3_OUT_BF16 or T3_OUT_F32_ADD
+  const float* row_scale; // [out_rows] or null (ones)
+  const float* col_scale; // [out_cols] or null (ones)
   int* err;
 };
+
+// Scaled epilogue: y = ((float)x * rs) * cs per element, each product rounded
+// to nearest (no contraction); x is the accumulator, an exact integer in f32
+// when the reduction is one chunk.  Stages float (128-byte-swizzled rows of
+// 32 words, like the int32 path) or bf16 ([128][64 B], unswizzled).
+// cs: this block's 32 column scales, staged in shared memory.
+__device__ __forceinline__ void stage_scaled(uint8_t* buf, int srow, const uint32_t (&v)[32],
+                                             float rs, const float* cs, int kind) {
+  float y[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) y[e] = __fmul_rn(__fmul_rn(__uint_as_float(v[e]), rs), cs[e]);
+  if (kind == T3_OUT_BF16) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(y[8 * g + 2 * j], y[8 * g + 2 * j + 1]);
+        w[j] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      sts128(buf + srow * 64 + 16 * g, w[0], w[1], w[2], w[3]);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      sts128(buf + tc::sw128(srow, c), __float_as_uint(y[4 * c]), __float_as_uint(y[4 * c + 1]),
+             __float_as_uint(y[4 * c + 2]), __float_as_uint(y[4 * c + 3]));
+  }
+}
 
 // ---------------------------------------------------------------- cluster
 
@@ -369,6 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* opb = smem + L::off_opb;
   uint8_t* raw = smem + L::off_raw;
   uint8_t* stage_out = smem + L::off_out;
+  float* cs_tile = reinterpret_cast<float*>(smem + L::off_cs);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + RAW_STAGES;
@@ -587,6 +629,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
       const int row0 = tr * BMP + static_cast<int>(rank) * 128;
       const int64_t row = static_cast<int64_t>(row0) + srow;
+      const float rs =
+          (p.out_kind != kOutI32 && p.row_scale && row < p.out_rows) ? __ldg(p.row_scale + row) : 1.0f;
       for (int64_t c0 = 0; c0 < p.num_stages; c0 += kChunkStages) {
         ok = mbar_wait(&acc_full[ab], aph, abort_flag, p.err, code_base | 4);
         ok = named_bar_and(kEpiBarrier, 128, __all_sync(0xffffffffu, ok));
@@ -594,6 +638,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool first = (c0 == 0);
         if (p.use_tma_out && c0 == kChunkStages && epi_tid == 0) bulk_wait_group<0>();
+        if (p.out_kind != kOutI32) {
+          // the tile's column scales, once (the barrier above ends the previous
+          // tile's reads of them)
+          for (int j = epi_tid; j < BN; j += 128) {
+            const int64_t col = static_cast<int64_t>(tcol) * BN + j;
+            cs_tile[j] = p.col_scale ? (col < p.out_cols ? __ldg(p.col_scale + col) : 0.0f) : 1.0f;
+          }
+          named_bar_sync(kEpiBarrier, 128);
+        }
         for (int cb = 0; cb < BN / 32; ++cb) {
           const int64_t col0 = static_cast<int64_t>(tcol) * BN + cb * 32;
           if (col0 >= p.out_cols) break;
@@ -613,20 +666,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint8_t* buf = stage_out + (slab & 1) * L::stage_out;
             if (epi_tid == 0) bulk_wait_group_read<1>();
             named_bar_sync(kEpiBarrier, 128);
+            if (p.out_kind == kOutI32) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int4 val =
-                  make_int4(tc::f32_bits_to_i32(v[4 * c]), tc::f32_bits_to_i32(v[4 * c + 1]),
-                            tc::f32_bits_to_i32(v[4 * c + 2]), tc::f32_bits_to_i32(v[4 * c + 3]));
-              sts128(buf + tc::sw128(srow, c), val);
+              for (int c = 0; c < 8; ++c) {
+                const int4 val =
+                    make_int4(tc::f32_bits_to_i32(v[4 * c]), tc::f32_bits_to_i32(v[4 * c + 1]),
+                              tc::f32_bits_to_i32(v[4 * c + 2]), tc::f32_bits_to_i32(v[4 * c + 3]));
+                sts128(buf + tc::sw128(srow, c), val);
+              }
+            } else {
+              stage_scaled(buf, srow, v, rs, cs_tile + cb * 32, p.out_kind);
             }
             fence_proxy_async_smem();
             named_bar_sync(kEpiBarrier, 128);
             if (epi_tid == 0) {
-              if (first)
-                tma_store_2d(&map_out, buf, static_cast<int>(col0), row0);
-              else
+              // the tensor map carries the element type: int32, f32 or bf16
+              if ((p.out_kind == kOutI32 && !first) || p.out_kind == T3_OUT_F32_ADD)
                 tma_reduce_add_2d(&map_out, buf, static_cast<int>(col0), row0);
+              else
+                tma_store_2d(&map_out, buf, static_cast<int>(col0), row0);
               bulk_commit_group();
             }
             ++slab;

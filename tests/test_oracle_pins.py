@@ -263,3 +263,73 @@ def test_dw_swaps_with_transposes():
     A = t3_synth.int8_uniform(g, (M, K))
     dY = t3_synth.int8_uniform(g, (M, N))
     assert np.array_equal(oracle.dw(A, dY).T, oracle.dw(dY, A))
+
+
+# ---------------------------------------------------------------- scaled outputs
+# The scaled outputs restate a definition (float32 steps, bf16 rounding to
+# nearest even); these pins check the oracle's numpy arithmetic against
+# independent computations: torch's own bf16 conversion, and exact rational
+# arithmetic rounded once per step.
+
+def _f32_round(q) -> np.float32:
+    """Nearest float32 (ties to even) of an exact rational whose float64
+    value is exact (every case below keeps it so)."""
+    return np.float32(float(q))
+
+
+def test_bf16_rounding_matches_torch_conversion():
+    torch = pytest.importorskip("torch")
+    g = np.random.default_rng(5)
+    y = np.concatenate([
+        g.standard_normal(20000).astype(np.float32) * np.float32(1e3),
+        # exact ties: a bf16 value plus half of its last place, both parities
+        (np.arange(1, 513, dtype=np.float32) * np.float32(2.0 ** -7) + np.float32(1.0)
+         + np.float32(2.0 ** -9)),
+        np.array([0.0, -0.0, 1.0, -1.0, 3.0e38, -3.0e38, 1e-40, 65504.0], dtype=np.float32),
+    ]).astype(np.float32)
+    ref = torch.from_numpy(y).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(oracle.bf16_bits(y), ref)
+
+
+def test_bf16_rounding_hand_values():
+    # 1 + 2^-8 lies halfway between bf16 1.0 (0x3F80) and 1 + 2^-7: ties to even
+    y = np.array([1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -2.5, 1.0 + 2.0 ** -8 + 2.0 ** -20],
+                 dtype=np.float32)
+    assert list(oracle.bf16_bits(y)) == [0x3F80, 0x3F80, 0x3F82, 0xC020, 0x3F81]
+
+
+def test_dequant_steps_match_exact_rationals():
+    from fractions import Fraction
+    g = np.random.default_rng(6)
+    rows, cols = 7, 9
+    x = g.integers(-2 ** 31, 2 ** 31, (rows, cols), dtype=np.int64).astype(np.int32)
+    x[0, :4] = [16777217, -16777219, 2 ** 24 + 3, 0]  # conversions that must round
+    rs = (g.standard_normal(rows) * 3).astype(np.float32)
+    cs = (g.standard_normal(cols) / 7).astype(np.float32)
+    old = (g.standard_normal((rows, cols)) * 1e6).astype(np.float32)
+    y = oracle.dequant(x, rs, cs)
+    add = oracle.dequant(x, rs, cs, oracle.OUT_F32_ADD, old)
+    for r in range(rows):
+        for c in range(cols):
+            xf = _f32_round(Fraction(int(x[r, c])))
+            t = _f32_round(Fraction(float(xf)) * Fraction(float(rs[r])))
+            want = _f32_round(Fraction(float(t)) * Fraction(float(cs[c])))
+            if want == 0:  # rationals have no signed zero: IEEE gives the product of the signs
+                want = np.float32(-0.0) if (np.signbit(xf) ^ np.signbit(rs[r]) ^ np.signbit(cs[c])) \
+                    else np.float32(0.0)
+            assert y[r, c] == want and np.signbit(y[r, c]) == np.signbit(want)
+            assert add[r, c] == _f32_round(Fraction(float(old[r, c])) + Fraction(float(want)))
+
+
+def test_dequant_special_cases():
+    x = np.array([[0, 5, -7, 2 ** 24 + 1]], dtype=np.int32)
+    # no scales: the nearest float of x
+    np.testing.assert_array_equal(oracle.dequant(x), np.array([[0, 5, -7, 2 ** 24]], np.float32))
+    # a negative scale turns 0 into -0.0
+    z = oracle.dequant(x, np.array([-1.0], np.float32))
+    assert z[0, 0] == 0.0 and np.signbit(z[0, 0])
+    # "+=" with an old value of 0 is the plain output; bf16 of small integers is exact
+    old = np.zeros((1, 4), np.float32)
+    np.testing.assert_array_equal(oracle.dequant(x, kind=oracle.OUT_F32_ADD, out=old), oracle.dequant(x))
+    b = oracle.dequant(np.array([[1, -2, 128]], np.int32), kind=oracle.OUT_BF16)
+    assert list(b[0]) == [0x3F80, 0xC000, 0x4300]
