@@ -247,12 +247,17 @@ def bench_scaled(t3, torch, dev, stream, A_d, wp_d, dY_d, K, reps=10):
     C = torch.empty((M, N), dtype=torch.float32, device=dev)
     dX = torch.empty((M, K), dtype=torch.float32, device=dev)
     dW = torch.empty((K, N), dtype=torch.float32, device=dev)
+    dW16 = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty((K, N), dtype=torch.int32, device=dev)
     calls = {
         "fwd": lambda: t3.t3_gemm_fwd_scaled(A_d, wp_d, K, rs_m, cs_n, t3.T3_OUT_F32, C=C, stream=stream),
         "dx": lambda: t3.t3_gemm_bwd_dx_scaled(dY_d, wp_d, K, rs_m, cs_k, t3.T3_OUT_F32, dX=dX,
                                                stream=stream),
         "dw": lambda: t3.t3_gemm_bwd_dw_scaled(A_d, dY_d, rs_k, cs_n, t3.T3_OUT_F32, dW=dW,
                                                stream=stream),
+        # bf16 dW: the exact int32 product goes through a caller-owned workspace
+        "dw_bf16_workspace": lambda: t3.t3_gemm_bwd_dw_scaled(
+            A_d, dY_d, rs_k, cs_n, t3.T3_OUT_BF16, dW=dW16, workspace=ws, stream=stream),
     }
     out = {}
     for name, call in calls.items():
