@@ -171,6 +171,28 @@ int t3_gemm_bwd_dw_scaled(const int8_t* A, const int8_t* dY, void* dW, int64_t M
                           int64_t K, const float* row_scale, const float* col_scale, int out_kind,
                           int32_t* workspace, t3_stream_t stream);
 
+/*
+ * t3_gemm_bwd_dw_scaled_noalloc -- t3_gemm_bwd_dw_scaled whose int32
+ * intermediate lives in a fixed buffer inside the library instead of a
+ * caller workspace, so that neither the call nor the caller allocates device
+ * memory for it.  The pages have no counterpart: it serves callers that
+ * cannot provide a workspace (bf16 and "+=" outputs need one).
+ *   The buffer holds 8,388,608 int32 entries (32 MiB) per device: K * N above
+ *   that returns T3_EINVAL before any CUDA call.  Nothing in it has to start
+ *   at zero (the dW product writes all of its K x N block first).
+ *   Races: every call on a device shares the buffer, so two calls must not
+ *   overlap on one device -- not on different streams, and not from several
+ *   host threads without ordering; each call's stream order alone protects
+ *   only calls on that stream.
+ *   The first call on each device resolves the buffer's address
+ *   (cudaGetSymbolAddress); make that call outside any stream capture.
+ * Arguments, sizes, results and other errors are those of
+ * t3_gemm_bwd_dw_scaled.
+ */
+int t3_gemm_bwd_dw_scaled_noalloc(const int8_t* A, const int8_t* dY, void* dW, int64_t M,
+                                  int64_t N, int64_t K, const float* row_scale,
+                                  const float* col_scale, int out_kind, t3_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* t3_status_string(int status);
 

@@ -72,6 +72,8 @@ def load():
             f = getattr(lib, name)
             f.argtypes = [p, p, p, i64, i64, i64, p, p, ctypes.c_int, p, p]
             f.restype = ctypes.c_int
+        lib.t3_gemm_bwd_dw_scaled_noalloc.argtypes = [p, p, p, i64, i64, i64, p, p, ctypes.c_int, p]
+        lib.t3_gemm_bwd_dw_scaled_noalloc.restype = ctypes.c_int
         lib.t3_status_string.argtypes = [ctypes.c_int]
         lib.t3_status_string.restype = ctypes.c_char_p
         lib.t3_last_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
@@ -319,6 +321,25 @@ def t3_gemm_bwd_dw_scaled(A, dY, row_scale=None, col_scale=None, kind=T3_OUT_F32
     with torch.cuda.device(A.device):
         rc = load().t3_gemm_bwd_dw_scaled(*args)
     _check(rc, "t3_gemm_bwd_dw_scaled")
+    return dW
+
+
+def t3_gemm_bwd_dw_scaled_noalloc(A, dY, row_scale=None, col_scale=None, kind=T3_OUT_F32,
+                                  dW=None, stream=None):
+    """t3_gemm_bwd_dw_scaled with the int32 intermediate in the library's fixed
+    per-device buffer (K * N <= 8,388,608; calls on one device must not overlap)."""
+    torch = _torch()
+    M, K = A.shape
+    if dY.shape[0] != M:
+        raise ValueError("A and dY must have the same number of rows")
+    N = dY.shape[1]
+    dW, pw = _scaled_out(dW, kind, K, N, A.device, "dW")
+    args = (_dev_ptr(A, torch.int8, "A"), _dev_ptr(dY, torch.int8, "dY"), pw, M, N, K,
+            _scale_ptr(row_scale, K, "row_scale"), _scale_ptr(col_scale, N, "col_scale"), kind,
+            _stream(A, stream))
+    with torch.cuda.device(A.device):
+        rc = load().t3_gemm_bwd_dw_scaled_noalloc(*args)
+    _check(rc, "t3_gemm_bwd_dw_scaled_noalloc")
     return dW
 
 

@@ -435,6 +435,45 @@ int t3_gemm_bwd_dw_scaled(const int8_t* A, const int8_t* dY, void* dW, int64_t M
       col_scale, out_kind, workspace, stream);
 }
 
+}  // extern "C"
+
+namespace t3 {
+namespace {
+
+// The int32 intermediate of t3_gemm_bwd_dw_scaled_noalloc: a fixed device
+// buffer of 8 Mi entries (32 MiB) per device, enough for dW up to K * N =
+// 8,388,608 (the 1280 x 3456 layer's dW has 4,423,680).  Nothing in it has to
+// start at zero: the dW product writes every entry of its K x N block before
+// the dequantization reads it.  Every call on a device shares it.
+constexpr int64_t kNoAllocWorkspaceEntries = 8LL * 1024 * 1024;
+std::atomic<int32_t*> g_noalloc_addr[kMaxDevices];  // resolved once per device
+
+}  // namespace
+
+static __device__ __align__(256) int32_t g_noalloc_workspace[kNoAllocWorkspaceEntries];
+
+}  // namespace t3
+
+extern "C" {
+
+int t3_gemm_bwd_dw_scaled_noalloc(const int8_t* A, const int8_t* dY, void* dW, int64_t M,
+                                  int64_t N, int64_t K, const float* row_scale,
+                                  const float* col_scale, int out_kind, t3_stream_t stream) {
+  if (bad_dims(M, N, K) || !valid_out_kind(out_kind)) return T3_EINVAL;
+  if (K == 0 || N == 0) return T3_OK;
+  if (K * N > kNoAllocWorkspaceEntries) return T3_EINVAL;  // checked before any CUDA call
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return T3_EDEVICE;
+  int32_t* ws = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (!ws) {
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ws), g_noalloc_workspace) != cudaSuccess)
+      return T3_ECUDA;
+    g_noalloc_addr[dev].store(ws, std::memory_order_release);
+  }
+  return t3_gemm_bwd_dw_scaled(A, dY, dW, M, N, K, row_scale, col_scale, out_kind, ws, stream);
+}
+
 const char* t3_status_string(int status) {
   switch (status) {
     case T3_OK: return "T3_OK: success";
