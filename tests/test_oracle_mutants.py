@@ -49,3 +49,89 @@ def test_pins_catch_planted_mistake(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
+
+
+# ------------------------------------------------ scaled outputs (numpy oracle)
+# Plausible mistakes in oracle.dequant / oracle.bf16_bits, swapped in with
+# monkeypatch; at least one of the scaled-output pins must fail for each.
+
+def _m_swapped_scale_order(x, row_scale=None, col_scale=None, kind=0, out=None):
+    import numpy as np
+    x = np.asarray(x, np.int32)
+    rows, cols = x.shape
+    rs = np.ones(rows, np.float32) if row_scale is None else np.asarray(row_scale, np.float32)
+    cs = np.ones(cols, np.float32) if col_scale is None else np.asarray(col_scale, np.float32)
+    y = (x.astype(np.float32) * cs[None, :]) * rs[:, None]
+    return _finish(y, kind, out)
+
+
+def _m_one_rounding(x, row_scale=None, col_scale=None, kind=0, out=None):
+    import numpy as np
+    x = np.asarray(x, np.int32)
+    rows, cols = x.shape
+    rs = np.ones(rows) if row_scale is None else np.asarray(row_scale, np.float64)
+    cs = np.ones(cols) if col_scale is None else np.asarray(col_scale, np.float64)
+    y = (x.astype(np.float64) * rs[:, None] * cs[None, :]).astype(np.float32)
+    return _finish(y, kind, out)
+
+
+def _m_add_before_scaling(x, row_scale=None, col_scale=None, kind=0, out=None):
+    import numpy as np
+    import oracle
+    if kind != oracle.OUT_F32_ADD:
+        return _ORIG_DEQUANT(x, row_scale, col_scale, kind, out)
+    x = np.asarray(x, np.int32)
+    rows, cols = x.shape
+    rs = np.ones(rows, np.float32) if row_scale is None else np.asarray(row_scale, np.float32)
+    cs = np.ones(cols, np.float32) if col_scale is None else np.asarray(col_scale, np.float32)
+    return ((np.asarray(out, np.float32) + x.astype(np.float32)) * rs[:, None]) * cs[None, :]
+
+
+def _m_bf16_truncates(y):
+    import numpy as np
+    u = np.ascontiguousarray(y, dtype=np.float32).view(np.uint32)
+    return (u >> 16).astype(np.uint16)
+
+
+def _m_bf16_ties_away(y):
+    import numpy as np
+    u = np.ascontiguousarray(y, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x8000) >> 16).astype(np.uint16)
+
+
+def _finish(y, kind, out):
+    import numpy as np
+    import oracle
+    if kind == oracle.OUT_F32:
+        return y
+    if kind == oracle.OUT_BF16:
+        return oracle.bf16_bits(y)
+    return np.asarray(out, np.float32) + y
+
+
+import oracle as _oracle_mod  # noqa: E402
+
+_ORIG_DEQUANT = _oracle_mod.dequant
+
+SCALED_MUTANTS = {
+    "dequant_swapped_scale_order": ("dequant", _m_swapped_scale_order),
+    "dequant_one_rounding_in_float64": ("dequant", _m_one_rounding),
+    "dequant_adds_before_scaling": ("dequant", _m_add_before_scaling),
+    "bf16_truncates": ("bf16_bits", _m_bf16_truncates),
+    "bf16_ties_away_from_zero": ("bf16_bits", _m_bf16_ties_away),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SCALED_MUTANTS))
+def test_scaled_pins_catch_planted_mistake(name, monkeypatch):
+    import test_oracle_pins as pins
+    attr, fn = SCALED_MUTANTS[name]
+    monkeypatch.setattr(_oracle_mod, attr, fn)
+    caught = 0
+    for pin in (pins.test_bf16_rounding_matches_torch_conversion, pins.test_bf16_rounding_hand_values,
+                pins.test_dequant_steps_match_exact_rationals, pins.test_dequant_special_cases):
+        try:
+            pin()
+        except AssertionError:
+            caught += 1
+    assert caught > 0, f"no scaled-output pin caught mutant {name}"
