@@ -310,6 +310,37 @@ def bench_device_pack(t3, torch, dev, stream, hbm_gbs, reps=20):
     return out
 
 
+def bench_quantize(t3, torch, dev, stream, hbm_gbs, M, K, reps=20):
+    """Row quantizer at the layer's activation shape: bytes moved (bf16 in,
+    int8 and row scales out) per call over its device time, inputs rotated
+    past the L2, calls replayed from a CUDA graph."""
+    g = torch.Generator(device="cpu").manual_seed(7)
+    x = (torch.randn((M, K), generator=g) * 3).to(torch.bfloat16).to(dev)
+    copies = max(2, -(-2 * 129 * 2**20 // (x.numel() * 2)))
+    xs = [x.clone() for _ in range(copies)]
+    q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    sc = torch.empty((M,), dtype=torch.float32, device=dev)
+    for i in range(3):
+        t3.t3_quantize_rows_bf16(xs[i % copies], q, sc, stream=stream)
+    torch.cuda.synchronize(dev)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        for i in range(reps):
+            t3.t3_quantize_rows_bf16(xs[i % copies], q, sc)
+    gr.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    gr.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    nbytes = M * K * 2 + M * K + M * 4
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"M": M, "K": K, "us_per_call": round(us, 3), "bytes": nbytes, "GBps": round(gbs, 1),
+            "frac_hbm": round(gbs / hbm_gbs, 3), "timing": "graph"}
+
+
 def cpu_baseline(A, w, dY, target_s=15.0):
     """The oracle, as it stands, on a bounded sample of rows of each product."""
     import oracle
@@ -540,6 +571,7 @@ def main():
     }
     hbm = peaks.get("hbm_gbs", 6800.0) if peak_src == "measured" else 6800.0
     line["scaled_f32"] = bench_scaled(t3, torch, dev, stream, A_d, wp_d, dY_d, K)
+    line["quantize_rows"] = bench_quantize(t3, torch, dev, stream, hbm, M, K)
     if not args.no_pack:
         line["device_pack"] = {"hbm_peak_GBps": hbm, "calls": bench_device_pack(t3, torch, dev, stream, hbm)}
     if not args.no_small_m:

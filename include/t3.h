@@ -121,6 +121,24 @@ int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, in
                    int64_t K, t3_stream_t stream);
 
 /*
+ * t3_quantize_rows_bf16 -- the step before the products: bf16 activations to
+ * int8 with one scale per row.  The second page feeds its int8 kernels from
+ * quantized tensors and names per-row scales for dX but gives no quantizer;
+ * this is symmetric absmax per row:
+ *   amax = max_k |x[m][k]|, row_scale[m] = amax / 127, inv = 127 / amax
+ *   (each a float division rounded to nearest),
+ *   q[m][k] = rint(x[m][k] * inv)  (product rounded to a float, then to the
+ *   nearest integer, ties to even), clamped to [-127, 127];
+ *   a row of zeros gives q = 0 and row_scale = 0.
+ *   x DEVICE bf16 [M][K] (bit patterns), q DEVICE int8 [M][K], row_scale
+ *   DEVICE float [M]; all owned by the caller.  Finite inputs; a product
+ *   0 * inf (amax so small that 127 / amax overflows) counts as 0.
+ * Asynchronous on `stream`.  M = 0 is a no-op; K = 0 writes row_scale = 0.
+ */
+int t3_quantize_rows_bf16(const void* x, int8_t* q, float* row_scale, int64_t M, int64_t K,
+                          t3_stream_t stream);
+
+/*
  * Scaled outputs -- the step after the products in "spec(igla): hslm_bwd_ptx
  * -- HSLM backward dX and dW as int8 tensor-core PTX written by t27": the
  * host rescales the integer results (dX by a scale per row; dW by scales per

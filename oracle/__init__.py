@@ -225,6 +225,29 @@ def dequant(x, row_scale=None, col_scale=None, kind: int = OUT_F32, out=None) ->
     raise ValueError(f"unknown output kind {kind}")
 
 
+def quantize_rows(x_bits):
+    """bf16 activations (bit patterns, uint16 [M][K]) -> (int8 q [M][K], float32
+    scale [M]): the step before the products, symmetric absmax per row (the
+    second page names per-row scales for dX but gives no quantizer).
+    amax = max |x|; scale = amax / 127 and inv = 127 / amax as float32
+    divisions; q = rint(x * inv) with the product rounded to float32 and rint
+    to nearest, ties to even, clamped to [-127, 127]; zero rows give q = 0,
+    scale = 0; a product 0 * inf counts as 0."""
+    u = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = u.shape
+    x = (u.astype(np.uint32) << 16).view(np.float32)
+    amax = np.abs(x).max(axis=1) if K else np.zeros(M, np.float32)
+    pos = amax > 0
+    safe = np.where(pos, amax, np.float32(1))
+    scale = np.where(pos, safe / np.float32(127), np.float32(0)).astype(np.float32)
+    with np.errstate(over="ignore", invalid="ignore"):
+        inv = np.where(pos, np.float32(127) / safe, np.float32(0)).astype(np.float32)
+        prod = x * inv[:, None]
+    prod = np.where(np.isnan(prod), np.float32(0), prod)
+    q = np.clip(np.rint(prod), -127, 127).astype(np.int8)
+    return q, scale
+
+
 def num_threads() -> int:
     """Threads the oracle's OpenMP loops run on."""
     return _load().oracle_num_threads()

@@ -11,6 +11,7 @@ Function names follow the C ABI:
   t3_gemm_fwd(A, Wp, K=None, C=None)       C  = A . W        (int32 [M][N])
   t3_gemm_bwd_dx(dY, Wp, K, dX=None)       dX = dY . W^T     (int32 [M][K])
   t3_gemm_bwd_dw(A, dY, dW=None)           dW = A^T . dY     (int32 [K][N])
+  t3_quantize_rows_bf16(x)                 (int8 q, per-row scale) from bf16 x
   t3_dequant_i32(x, kind, row_scale, col_scale, out=None)   scaled float/bf16 output
   t3_gemm_fwd_scaled / t3_gemm_bwd_dx_scaled / t3_gemm_bwd_dw_scaled
                                            the products with that output
@@ -66,6 +67,8 @@ def load():
         lib.t3_pack_ternary.restype = ctypes.c_int
         lib.t3_pack_ternary_device.argtypes = [p, p, i64, i64, p]
         lib.t3_pack_ternary_device.restype = ctypes.c_int
+        lib.t3_quantize_rows_bf16.argtypes = [p, p, p, i64, i64, p]
+        lib.t3_quantize_rows_bf16.restype = ctypes.c_int
         lib.t3_dequant_i32.argtypes = [p, p, i64, i64, p, p, ctypes.c_int, p]
         lib.t3_dequant_i32.restype = ctypes.c_int
         for name in ("t3_gemm_fwd_scaled", "t3_gemm_bwd_dx_scaled", "t3_gemm_bwd_dw_scaled"):
@@ -251,6 +254,27 @@ def _ws_ptr(ws, rows, cols):
     if tuple(ws.shape) != (rows, cols):
         raise ValueError(f"workspace must be [{rows}][{cols}]")
     return _dev_ptr(ws, _torch().int32, "workspace")
+
+
+def t3_quantize_rows_bf16(x, q=None, row_scale=None, stream=None):
+    """(q, row_scale): bf16 x [M][K] quantized to int8 with one absmax scale
+    per row (see include/t3.h)."""
+    torch = _torch()
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise TypeError("x must be a 2-D CUDA bfloat16 tensor [M][K]")
+    M, K = x.shape
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if row_scale is None:
+        row_scale = torch.empty((M,), dtype=torch.float32, device=x.device)
+    if tuple(q.shape) != (M, K) or tuple(row_scale.shape) != (M,):
+        raise ValueError("q must be [M][K] and row_scale [M]")
+    args = (_dev_ptr(x, torch.bfloat16, "x"), _dev_ptr(q, torch.int8, "q"),
+            _dev_ptr(row_scale, torch.float32, "row_scale"), M, K, _stream(x, stream))
+    with torch.cuda.device(x.device):
+        rc = load().t3_quantize_rows_bf16(*args)
+    _check(rc, "t3_quantize_rows_bf16")
+    return q, row_scale
 
 
 def t3_dequant_i32(x, kind=T3_OUT_F32, row_scale=None, col_scale=None, out=None, stream=None):

@@ -375,6 +375,17 @@ int t3_pack_ternary_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N,
   return launch_pack_device(w, wp, K, N, dev->sms, dev->err_word, stream);
 }
 
+int t3_quantize_rows_bf16(const void* x, int8_t* q, float* row_scale, int64_t M, int64_t K,
+                          t3_stream_t stream) {
+  if (M < 0 || K < 0 || M > kMaxDim || K > kMaxDim) return T3_EINVAL;
+  if (M == 0) return T3_OK;
+  if (!row_scale || (K > 0 && (!x || !q))) return T3_EINVAL;
+  const DeviceInfo* dev = nullptr;
+  const int st = device_info(&dev);
+  if (st != T3_OK) return st;
+  return launch_quant_rows(x, q, row_scale, M, K, dev->sms, stream);
+}
+
 int t3_dequant_i32(const int32_t* x, void* out, int64_t rows, int64_t cols,
                    const float* row_scale, const float* col_scale, int out_kind,
                    t3_stream_t stream) {

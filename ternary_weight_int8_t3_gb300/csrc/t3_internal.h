@@ -46,6 +46,10 @@ int launch_dw2(const dw2::Params& p, const CUtensorMap& ma, const CUtensorMap& m
 int launch_pack_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N, int sms, int* err,
                        cudaStream_t s);
 
+// bf16 x [M][K] -> int8 q [M][K] and a float scale per row (absmax), on `s`.
+int launch_quant_rows(const void* x, int8_t* q, float* scale, int64_t M, int64_t K, int sms,
+                      cudaStream_t s);
+
 // out[r][c] = scaled int32 x[r][c] (T3_OUT_* kind), on `s`.
 int launch_dequant(const int32_t* x, void* out, int64_t rows, int64_t cols, const float* row_scale,
                    const float* col_scale, int kind, int sms, cudaStream_t s);

@@ -135,3 +135,47 @@ def test_scaled_pins_catch_planted_mistake(name, monkeypatch):
         except AssertionError:
             caught += 1
     assert caught > 0, f"no scaled-output pin caught mutant {name}"
+
+
+def _quant_mutant(ties_away=False, divisor=127.0, inv64=False, lo=-127, hi=127):
+    def quantize_rows(x_bits):
+        import numpy as np
+        u = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        M, K = u.shape
+        x = (u.astype(np.uint32) << 16).view(np.float32)
+        amax = np.abs(x).max(axis=1) if K else np.zeros(M, np.float32)
+        pos = amax > 0
+        safe = np.where(pos, amax, np.float32(1))
+        scale = np.where(pos, safe / np.float32(divisor), 0).astype(np.float32)
+        if inv64:
+            inv = np.where(pos, 127.0 / safe.astype(np.float64), 0.0)
+            prod = (x.astype(np.float64) * inv[:, None])
+        else:
+            inv = np.where(pos, np.float32(divisor) / safe, 0).astype(np.float32)
+            prod = x * inv[:, None]
+        r = np.floor(prod + 0.5) if ties_away else np.rint(prod)
+        return np.clip(r, lo, hi).astype(np.int8), scale
+    return quantize_rows
+
+
+QUANT_MUTANTS = {
+    "quant_ties_rounded_up": _quant_mutant(ties_away=True),
+    "quant_divides_by_128": _quant_mutant(divisor=128.0),
+    "quant_product_in_float64": _quant_mutant(inv64=True),
+    "quant_clamps_to_126": _quant_mutant(lo=-126, hi=126),
+}
+
+
+@pytest.mark.parametrize("name", sorted(QUANT_MUTANTS))
+def test_quantizer_pins_catch_planted_mistake(name, monkeypatch):
+    import test_oracle_pins as pins
+    monkeypatch.setattr(_oracle_mod, "quantize_rows", QUANT_MUTANTS[name])
+    caught = 0
+    for pin in (pins.test_quantize_rows_hand_values_and_ties, pins.test_quantize_rows_against_exact_rationals,
+                pins.test_quantize_rows_float32_rounding_of_the_product,
+                pins.test_quantize_rows_properties):
+        try:
+            pin()
+        except AssertionError:
+            caught += 1
+    assert caught > 0, f"no quantizer pin caught mutant {name}"

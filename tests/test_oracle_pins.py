@@ -333,3 +333,86 @@ def test_dequant_special_cases():
     np.testing.assert_array_equal(oracle.dequant(x, kind=oracle.OUT_F32_ADD, out=old), oracle.dequant(x))
     b = oracle.dequant(np.array([[1, -2, 128]], np.int32), kind=oracle.OUT_BF16)
     assert list(b[0]) == [0x3F80, 0xC000, 0x4300]
+
+
+# ------------------------------------------------------------ row quantizer
+
+def _bf16(values):
+    return (np.asarray(values, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _f32_nearest_even(q):
+    """The float32 nearest to the rational q (ties to even), by integer
+    arithmetic on the exact value; normal range."""
+    from fractions import Fraction
+    if q == 0:
+        return np.float32(0.0)
+    sign = -1 if q < 0 else 1
+    a = abs(Fraction(q))
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if a >= Fraction(2) ** e:   # now 2^e <= a < 2^(e+1)
+        pass
+    else:
+        e -= 1
+    scaled = a / Fraction(2) ** (e - 23)   # in [2^23, 2^24)
+    m, rem = divmod(scaled.numerator, scaled.denominator)
+    twice = 2 * rem
+    if twice > scaled.denominator or (twice == scaled.denominator and m % 2 == 1):
+        m += 1
+    return np.float32(sign * float(Fraction(m) * Fraction(2) ** (e - 23)))
+
+
+def test_quantize_rows_hand_values_and_ties():
+    q, s = oracle.quantize_rows(np.stack([_bf16([1, -2, 0.5, 127]), _bf16([0, 0, 0, 0]),
+                                          _bf16([0.75, 1.5, 2.5, -127])]))
+    assert q.tolist() == [[1, -2, 0, 127], [0, 0, 0, 0], [1, 2, 2, -127]]
+    assert s.tolist() == [1.0, 0.0, 1.0]
+
+
+def test_quantize_rows_against_exact_rationals():
+    from fractions import Fraction
+    g = np.random.default_rng(11)
+    x = (g.standard_normal((12, 37)) * np.float32(10.0) ** g.integers(-3, 4, (12, 1))).astype(np.float32)
+    bits = _bf16(x)
+    q, s = oracle.quantize_rows(bits)
+    xf = (bits.astype(np.uint32) << 16).view(np.float32)
+    for m in range(12):
+        amax = max(abs(float(v)) for v in xf[m])
+        assert s[m] == _f32_nearest_even(Fraction(amax) / 127)
+        inv = _f32_nearest_even(Fraction(127) / Fraction(amax))
+        for k in range(37):
+            prod = _f32_nearest_even(Fraction(float(xf[m, k])) * Fraction(float(inv)))
+            fl = Fraction(float(prod))
+            r = round(fl)  # Python rounds halves to even
+            assert q[m, k] == max(-127, min(127, r))
+
+
+def _exact_chain_q(xf, amax):
+    from fractions import Fraction
+    inv = _f32_nearest_even(Fraction(127) / Fraction(amax))
+    prod = _f32_nearest_even(Fraction(xf) * Fraction(float(inv)))
+    return max(-127, min(127, round(Fraction(float(prod)))))
+
+
+def test_quantize_rows_float32_rounding_of_the_product():
+    # x = amax / 2: the exact product is 63.5, and the float32 roundings of
+    # 127 / amax and of x * inv decide between 63 and 64 (found by search)
+    pairs = [(0.00982666015625, 0.0196533203125), (0.0128173828125, 0.025634765625),
+             (0.01409912109375, 0.0281982421875), (0.0279541015625, 0.055908203125),
+             (0.048583984375, 0.09716796875), (0.05029296875, 0.1005859375)]
+    q, _ = oracle.quantize_rows(np.stack([_bf16([x, amax]) for x, amax in pairs]))
+    assert [int(v) for v in q[:, 0]] == [_exact_chain_q(x, amax) for x, amax in pairs]
+    assert sorted(set(int(v) for v in q[:, 0])) == [63, 64]
+
+
+def test_quantize_rows_properties():
+    g = np.random.default_rng(12)
+    x = (g.standard_normal((64, 300)) * 3).astype(np.float32)
+    bits = _bf16(x)
+    q, s = oracle.quantize_rows(bits)
+    xf = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.abs(q.astype(int)).max() <= 127
+    am = np.abs(xf).argmax(axis=1)
+    assert np.all(np.abs(q[np.arange(64), am]) == 127)       # the row's maximum maps to +-127
+    err = np.abs(q * s[:, None].astype(np.float64) - xf)
+    assert np.all(err <= s[:, None] * 0.5 * (1 + 1e-5))       # half a step, plus float slack
