@@ -195,7 +195,11 @@ int run_tc2(const int8_t* act, const uint8_t* Wp, void* out, int64_t M, int64_t 
   const bool w_ok = (OP == kOpFwd)
                         ? make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BNH, tc2::BK / 4)
                         : make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BK, tc2::BN / 4);
-  if (!w_ok) return T3_EINVAL;
+  // Wp rows that are 4-byte but not 16-byte aligned: the weight decoders load
+  // their words themselves (the map is then unused: a copy of the activations')
+  const bool w_words = !w_ok && KB % 4 == 0 && reinterpret_cast<uintptr_t>(Wp) % 4 == 0;
+  if (!w_ok && !w_words) return T3_EINVAL;
+  if (!w_ok) mw = ma;
   if (!make_out_map(&mo, out, M, out_cols, out_kind)) return T3_EINVAL;
   if (out_kind != tc2::kOutI32 && ceil_div(act_cols, tc2::BK) > tc2::kChunkStages) return T3_EINVAL;
   tc2::Params p{};
@@ -214,6 +218,9 @@ int run_tc2(const int8_t* act, const uint8_t* Wp, void* out, int64_t M, int64_t 
   p.out_kind = out_kind;
   p.row_scale = row_scale;
   p.col_scale = col_scale;
+  p.wp = Wp;
+  p.kb_bytes = KB;
+  p.w_tma = w_ok ? 1 : 0;
   p.err = dev->err_word;
   const int64_t pairs = std::min<int64_t>(tiles_r * tiles_c, dev->sms / 2);
   const int grid = static_cast<int>(2 * pairs);

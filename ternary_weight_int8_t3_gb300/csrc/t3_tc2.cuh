@@ -98,6 +98,11 @@ struct Params {
   int out_kind;           // kOutI32, T3_OUT_F32, T3_OUT_BF16 or T3_OUT_F32_ADD
   const float* row_scale; // [out_rows] or null (ones)
   const float* col_scale; // [out_cols] or null (ones)
+  // Wp rows a TMA map cannot describe (ceil(K/4) not a multiple of 16 bytes,
+  // but of 4): the weight decoders then load their words from global memory
+  const uint8_t* wp;
+  int64_t kb_bytes;       // ceil(K/4), the row stride of Wp
+  int w_tma;              // 1: weights come by TMA with the activations
   int* err;
 };
 
@@ -292,25 +297,31 @@ __device__ __forceinline__ void fwd_word_unit(int tid, int i, int& row, int& w) 
   w = (wl & 3) + 4 * (wl >> 4);
 }
 
+// One word of 16 codes -> 8 f16x2 words: its even codes (4 words), then its
+// odd codes.
+__device__ __forceinline__ void decode_word_f16(uint32_t x, uint32_t* v) {
+  const uint32_t e = x & 0x33333333u, o = (x >> 2) & 0x33333333u;
+  const uint32_t he0 = prmt(tc::kF16HiTable, 0u, e);
+  const uint32_t he1 = prmt(tc::kF16HiTable, 0u, e >> 16);
+  const uint32_t ho0 = prmt(tc::kF16HiTable, 0u, o);
+  const uint32_t ho1 = prmt(tc::kF16HiTable, 0u, o >> 16);
+  v[0] = prmt(he0, 0u, 0x1404u);
+  v[1] = prmt(he0, 0u, 0x3424u);
+  v[2] = prmt(he1, 0u, 0x1404u);
+  v[3] = prmt(he1, 0u, 0x3424u);
+  v[4] = prmt(ho0, 0u, 0x1404u);
+  v[5] = prmt(ho0, 0u, 0x3424u);
+  v[6] = prmt(ho1, 0u, 0x1404u);
+  v[7] = prmt(ho1, 0u, 0x3424u);
+}
+
 __device__ __forceinline__ void w_fwd_load(const uint8_t* raw_w, int tid, uint32_t (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < kFwdWordsPerThread; ++i) {
     int row, w;
     fwd_word_unit(tid, i, row, w);
     const uint32_t x = *reinterpret_cast<const uint32_t*>(raw_w + row * 32 + 4 * w);
-    const uint32_t e = x & 0x33333333u, o = (x >> 2) & 0x33333333u;
-    const uint32_t he0 = prmt(tc::kF16HiTable, 0u, e);
-    const uint32_t he1 = prmt(tc::kF16HiTable, 0u, e >> 16);
-    const uint32_t ho0 = prmt(tc::kF16HiTable, 0u, o);
-    const uint32_t ho1 = prmt(tc::kF16HiTable, 0u, o >> 16);
-    v[8 * i + 0] = prmt(he0, 0u, 0x1404u);
-    v[8 * i + 1] = prmt(he0, 0u, 0x3424u);
-    v[8 * i + 2] = prmt(he1, 0u, 0x1404u);
-    v[8 * i + 3] = prmt(he1, 0u, 0x3424u);
-    v[8 * i + 4] = prmt(ho0, 0u, 0x1404u);
-    v[8 * i + 5] = prmt(ho0, 0u, 0x3424u);
-    v[8 * i + 6] = prmt(ho1, 0u, 0x1404u);
-    v[8 * i + 7] = prmt(ho1, 0u, 0x3424u);
+    decode_word_f16(x, v + 8 * i);
   }
 }
 
@@ -365,19 +376,31 @@ __device__ __forceinline__ void w_dx_load(const uint8_t* raw_w, int tid, uint32_
     dx_word_unit(tid, i, n, j);
     const uint32_t x = *reinterpret_cast<const uint32_t*>(
         raw_w + n * (BN / 4) + 24 * static_cast<int>(rank) + 4 * j);
-    const uint32_t e = x & 0x33333333u, o = (x >> 2) & 0x33333333u;
-    const uint32_t he0 = prmt(tc::kF16HiTable, 0u, e);
-    const uint32_t he1 = prmt(tc::kF16HiTable, 0u, e >> 16);
-    const uint32_t ho0 = prmt(tc::kF16HiTable, 0u, o);
-    const uint32_t ho1 = prmt(tc::kF16HiTable, 0u, o >> 16);
-    v[8 * i + 0] = prmt(he0, 0u, 0x1404u);
-    v[8 * i + 1] = prmt(he0, 0u, 0x3424u);
-    v[8 * i + 2] = prmt(he1, 0u, 0x1404u);
-    v[8 * i + 3] = prmt(he1, 0u, 0x3424u);
-    v[8 * i + 4] = prmt(ho0, 0u, 0x1404u);
-    v[8 * i + 5] = prmt(ho0, 0u, 0x3424u);
-    v[8 * i + 6] = prmt(ho1, 0u, 0x1404u);
-    v[8 * i + 7] = prmt(ho1, 0u, 0x3424u);
+    decode_word_f16(x, v + 8 * i);
+  }
+}
+
+// The same words as w_fwd_load / w_dx_load read, from global memory (rows
+// 4-byte aligned, words past N rows or past ceil(K/4) bytes are 0, i.e. code 0).
+__device__ __forceinline__ void w_words_global(const Params& p, bool fwd, int tcol, int64_t kb,
+                                               uint32_t rank, int tid, uint32_t* x) {
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    int64_t n, off;
+    if (fwd) {
+      int row, w;
+      fwd_word_unit(tid, i, row, w);
+      n = static_cast<int64_t>(tcol) * BN + static_cast<int64_t>(rank) * BNH + row;
+      off = kb * (BK / 4) + 4 * w;
+    } else {
+      int nl, j;
+      dx_word_unit(tid, i, nl, j);
+      n = kb * BK + nl;
+      off = static_cast<int64_t>(tcol) * (BN / 4) + 24 * static_cast<int64_t>(rank) + 4 * j;
+    }
+    x[i] = (n < p.N && off < p.kb_bytes)
+               ? __ldg(reinterpret_cast<const uint32_t*>(p.wp + n * p.kb_bytes + off))
+               : 0u;
   }
 }
 
@@ -398,7 +421,7 @@ __device__ __forceinline__ void w_dx_store(uint8_t* opb, int tid, const uint32_t
 
 // ------------------------------------------------------------------ kernel
 
-template <int OP>
+template <int OP, bool kWGlobal>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc2_kernel(const Params p, const __grid_constant__ CUtensorMap map_a,
                const __grid_constant__ CUtensorMap map_w,
@@ -432,7 +455,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RAW_STAGES; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], kConvWarps);
+      // without weight TMA only the activation warps read the raw stages
+      mbar_init(&raw_empty[s], kWGlobal ? kActWarps : kConvWarps);
     }
     for (int s = 0; s < OP_STAGES; ++s) {
       mbar_init(&op_full[s], kConvWarps + 1);  // own converters + the odd CTA's forwarder
@@ -466,11 +490,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t* signal = (rank == 0) ? op_full : op_ready;  // local, CTA scope
     uint32_t rs = 0, rph = 0, os = 0, oph = 0;
     bool ok = true;
+    static_assert(kFwdWordsPerThread == 3 && kDxWordsPerThread == 3, "three words per thread");
+    // weights from global memory: this stage's words, loaded during the
+    // previous stage (while that one waited for its operand slot)
+    // kWGlobal: the instantiation for Wp rows without weight TMA (p.w_tma == 0)
+    const bool w_global = kWGlobal && !act_warp;
+    uint32_t wx[3] = {0u, 0u, 0u};
+    if (kWGlobal && w_global && pair < num_tiles)
+      w_words_global(p, OP == kOpFwd, pair % p.tiles_c, 0, rank, wtid, wx);
     for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
       for (int64_t kb = 0; kb < p.num_stages; ++kb) {
         const uint8_t* ra = raw + rs * L::raw_stage;
         const uint32_t act_taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kActCol +
                                    os * (BK / 2) + 32 * h;
+        if (kWGlobal && w_global) {
+          uint32_t v[32];
+#pragma unroll
+          for (int i = 0; i < 3; ++i) decode_word_f16(wx[i], v + 8 * i);
+          // the next stage's words go in flight now
+          const bool last_kb = kb + 1 == p.num_stages;
+          const int ntile = last_kb ? tile + npairs : tile;
+          if (ntile < num_tiles)
+            w_words_global(p, OP == kOpFwd, ntile % p.tiles_c, last_kb ? 0 : kb + 1, rank, wtid, wx);
+          ok = mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          if (OP == kOpFwd)
+            w_fwd_store(opb + os * L::opb_stage, wtid, v);
+          else
+            w_dx_store(opb + os * L::opb_stage, wtid, v);
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&signal[os]);
+          if (++rs == RAW_STAGES) { rs = 0; rph ^= 1u; }
+          if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
+          continue;
+        }
         // convert as soon as the raw stage is in, release it, and wait for the
         // operand slot only before storing: the two-slot ring runs latency-bound
         // on the slot hand-off, which the conversion then stays off
@@ -508,7 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&map_a);
-      prefetch_tensormap(&map_w);
+      if (!kWGlobal) prefetch_tensormap(&map_w);
     }
     uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
     bool ok = true;
@@ -530,12 +585,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (lane == 0) {
           uint8_t* dst = raw + stage * L::raw_stage;
-          mbar_arrive_expect_tx(&raw_full[stage], RAW_A + L::raw_w);
+          mbar_arrive_expect_tx(&raw_full[stage], RAW_A + (kWGlobal ? 0 : L::raw_w));
           tma_load_2d(dst, &map_a, &raw_full[stage], static_cast<int>(kb * BK), ay);
-          if (OP == kOpFwd)
-            tma_load_2d(dst + RAW_A, &map_w, &raw_full[stage], static_cast<int>(kb * (BK / 4)), wy);
-          else
-            tma_load_2d(dst + RAW_A, &map_w, &raw_full[stage], wx, static_cast<int>(kb * BK));
+          if (!kWGlobal) {
+            if (OP == kOpFwd)
+              tma_load_2d(dst + RAW_A, &map_w, &raw_full[stage], static_cast<int>(kb * (BK / 4)), wy);
+            else
+              tma_load_2d(dst + RAW_A, &map_w, &raw_full[stage], wx, static_cast<int>(kb * BK));
+          }
         }
         issued_mask |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);

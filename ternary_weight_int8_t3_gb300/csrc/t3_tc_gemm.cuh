@@ -133,22 +133,40 @@ __device__ __forceinline__ void box_coords(int tr, int tcol, int64_t kb, int& ax
 }
 
 // Plain-load copy of one box (rows x cols bytes) into shared memory with zero
-// fill outside the source: the producer's fallback when TMA is not allowed.
+// fill outside the source: the producer's fallback when TMA is not allowed
+// (rows of any alignment, so single-byte loads).  Each lane gathers 8 words
+// before storing any of them, so that their loads are in flight together
+// instead of one global round trip per word.
 __device__ __forceinline__ void manual_box(uint8_t* dst, const uint8_t* src, int64_t ld,
                                            int64_t src_rows, int64_t src_cols, int64_t y0,
                                            int64_t x0, int box_rows, int box_cols, int lane) {
+  constexpr int kBatch = 8;
   const int wpr = box_cols / 4;
-  for (int idx = lane; idx < box_rows * wpr; idx += 32) {
-    const int r = idx / wpr, cw = idx % wpr;
-    const int64_t y = y0 + r, x = x0 + 4 * cw;
-    uint32_t word = 0;
-    if (y < src_rows) {
-      const uint8_t* rowp = src + y * ld;
+  const int total = box_rows * wpr;
+  for (int base = lane; base < total; base += 32 * kBatch) {
+    uint32_t words[kBatch];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (x + j < src_cols) word |= static_cast<uint32_t>(__ldg(rowp + x + j)) << (8 * j);
+    for (int b = 0; b < kBatch; ++b) {
+      const int idx = base + 32 * b;
+      const int r = idx / wpr, cw = idx % wpr;
+      const int64_t y = y0 + r, x = x0 + 4 * cw;
+      uint32_t word = 0;
+      if (idx < total && y < src_rows) {
+        const uint8_t* rowp = src + y * ld;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (x + j < src_cols) word |= static_cast<uint32_t>(__ldg(rowp + x + j)) << (8 * j);
+      }
+      words[b] = word;
     }
-    *reinterpret_cast<uint32_t*>(dst + r * box_cols + 4 * cw) = word;
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int idx = base + 32 * b;
+      if (idx < total) {
+        const int r = idx / wpr, cw = idx % wpr;
+        *reinterpret_cast<uint32_t*>(dst + r * box_cols + 4 * cw) = words[b];
+      }
+    }
   }
 }
 

@@ -304,3 +304,15 @@ def test_empty_reduction_writes_zeros():
     t3.t3_gemm_fwd(torch.empty((5, 0), dtype=torch.int8, device="cuda"),
                    torch.empty((7, 0), dtype=torch.uint8, device="cuda"), K=0, C=C)
     assert torch.count_nonzero(C).item() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 1024, 4000), (300, 4000, 1008), (257, 336, 272)])
+def test_weight_rows_not_16_byte_aligned(M, N, K):
+    # ceil(K/4) a multiple of 4 but not of 16: the pair pipeline loads the
+    # weight words itself instead of by TMA
+    g = t3_synth.rng(M + N + K)
+    A = t3_synth.int8_uniform(g, (M, K))
+    dY = t3_synth.int8_uniform(g, (M, N))
+    wp = oracle.pack(t3_synth.ternary(g, (K, N)))
+    np.testing.assert_array_equal(run_fwd(A, wp), oracle.fwd(A, wp))
+    np.testing.assert_array_equal(run_dx(dY, wp, K), oracle.dx(dY, wp, K))
