@@ -191,16 +191,17 @@ int run_tc2(const int8_t* act, const uint8_t* Wp, void* out, int64_t M, int64_t 
   const int64_t act_cols = (OP == kOpFwd) ? K : N;
   const int64_t out_cols = (OP == kOpFwd) ? N : K;
   CUtensorMap ma, mw, mo;
-  if (!make_u8_map_tiled(&ma, act, M, act_cols, act_cols, 128, tc2::BK, true)) return T3_EINVAL;
+  // Operands TMA cannot address (row strides or bases not 16-byte aligned)
+  // are loaded by their converters from global memory instead; an int32
+  // output that cannot take bulk stores is written with plain stores.
+  const bool a_ok = make_u8_map_tiled(&ma, act, M, act_cols, act_cols, 128, tc2::BK, true);
   const bool w_ok = (OP == kOpFwd)
                         ? make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BNH, tc2::BK / 4)
                         : make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BK, tc2::BN / 4);
-  // Wp rows that are 4-byte but not 16-byte aligned: the weight decoders load
-  // their words themselves (the map is then unused: a copy of the activations')
-  const bool w_words = !w_ok && KB % 4 == 0 && reinterpret_cast<uintptr_t>(Wp) % 4 == 0;
-  if (!w_ok && !w_words) return T3_EINVAL;
+  const bool out_ok = make_out_map(&mo, out, M, out_cols, out_kind);
+  if (!out_ok && out_kind != tc2::kOutI32) return T3_EINVAL;  // scaled output needs bulk stores
+  if (!a_ok) ma = w_ok ? mw : mo;  // unused copies: any initialised map
   if (!w_ok) mw = ma;
-  if (!make_out_map(&mo, out, M, out_cols, out_kind)) return T3_EINVAL;
   if (out_kind != tc2::kOutI32 && ceil_div(act_cols, tc2::BK) > tc2::kChunkStages) return T3_EINVAL;
   tc2::Params p{};
   p.M = M;
@@ -214,13 +215,23 @@ int run_tc2(const int8_t* act, const uint8_t* Wp, void* out, int64_t M, int64_t 
   p.tiles_r = static_cast<int>(tiles_r);
   p.tiles_c = static_cast<int>(tiles_c);
   p.out = static_cast<int32_t*>(out);
-  p.use_tma_out = 1;
+  p.use_tma_out = out_ok ? 1 : 0;
   p.out_kind = out_kind;
   p.row_scale = row_scale;
   p.col_scale = col_scale;
   p.wp = Wp;
   p.kb_bytes = KB;
   p.w_tma = w_ok ? 1 : 0;
+  p.w_vec4 = (KB % 4 == 0) && (reinterpret_cast<uintptr_t>(Wp) % 4 == 0);
+  p.act = act;
+  p.act_rows = M;
+  p.act_cols = act_cols;
+  p.act_vec4 = (act_cols % 4 == 0) && (reinterpret_cast<uintptr_t>(act) % 4 == 0);
+  p.a_tma = a_ok ? 1 : 0;
+  // the weights-from-global instantiation loads whole words only
+  p.mode = (a_ok && w_ok) ? tc2::kModeTma
+           : (a_ok && p.w_vec4) ? tc2::kModeWGlobal
+                                : tc2::kModeAGlobal;
   p.err = dev->err_word;
   const int64_t pairs = std::min<int64_t>(tiles_r * tiles_c, dev->sms / 2);
   const int grid = static_cast<int>(2 * pairs);
@@ -236,10 +247,22 @@ int run_dw2(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N
   int st = device_info(&dev);
   if (st != T3_OK) return st;
   CUtensorMap ma, mdy, mo;
-  if (!make_u8_map_tiled(&ma, A, M, K, K, dw2::BK, 128)) return T3_EINVAL;
-  if (!make_u8_map_tiled(&mdy, dY, M, N, N, dw2::BK, 128)) return T3_EINVAL;
-  if (!make_i32_map_tiled(&mo, dW, K, N, 128, 32, true)) return T3_EINVAL;
+  // operands TMA cannot address are loaded by the converters themselves, and
+  // a dW that cannot take bulk adds gets per-element atomic adds
+  const bool a_ok = make_u8_map_tiled(&ma, A, M, K, K, dw2::BK, 128);
+  const bool dy_ok = make_u8_map_tiled(&mdy, dY, M, N, N, dw2::BK, 128);
+  const bool out_ok = make_i32_map_tiled(&mo, dW, K, N, 128, 32, true);
+  if (!a_ok) ma = dy_ok ? mdy : mo;  // unused copies: any initialised map
+  if (!dy_ok) mdy = ma;
+  if (!out_ok) mo = ma;
   dw2::Params p{};
+  p.a = A;
+  p.dy = dY;
+  p.a_vec4 = (K % 4 == 0) && (reinterpret_cast<uintptr_t>(A) % 4 == 0);
+  p.dy_vec4 = (N % 4 == 0) && (reinterpret_cast<uintptr_t>(dY) % 4 == 0);
+  p.out = dW;
+  p.use_tma_out = out_ok ? 1 : 0;
+  p.global_ops = (a_ok && dy_ok) ? 0 : 1;
   p.M = M;
   p.N = N;
   p.K = K;

@@ -103,8 +103,21 @@ struct Params {
   const uint8_t* wp;
   int64_t kb_bytes;       // ceil(K/4), the row stride of Wp
   int w_tma;              // 1: weights come by TMA with the activations
+  int w_vec4;             // Wp rows 4-byte aligned: word loads (else bytes)
+  // activation rows a TMA map cannot describe (their stride is not a
+  // multiple of 16 bytes): the activation converters load them themselves
+  const int8_t* act;      // [act_rows][act_cols]
+  int64_t act_rows, act_cols;
+  int act_vec4;           // activation rows 4-byte aligned: word loads (else bytes)
+  int a_tma;              // 1: activations come by TMA
+  int mode;               // kernel instantiation: kModeTma, kModeWGlobal, kModeAGlobal
   int* err;
 };
+
+// Kernel instantiations: all operands by TMA; weights from global memory as
+// whole words (activations by TMA); and the general one, where each operand
+// comes by TMA or from global memory as p.a_tma / p.w_tma say.
+constexpr int kModeTma = 0, kModeWGlobal = 1, kModeAGlobal = 2;
 
 // Scaled epilogue: y = ((float)x * rs) * cs per element, each product rounded
 // to nearest (no contraction); x is the accumulator, an exact integer in f32
@@ -382,6 +395,8 @@ __device__ __forceinline__ void w_dx_load(const uint8_t* raw_w, int tid, uint32_
 
 // The same words as w_fwd_load / w_dx_load read, from global memory (rows
 // 4-byte aligned, words past N rows or past ceil(K/4) bytes are 0, i.e. code 0).
+// kWords4: rows known to be 4-byte aligned (word loads only).
+template <bool kWords4>
 __device__ __forceinline__ void w_words_global(const Params& p, bool fwd, int tcol, int64_t kb,
                                                uint32_t rank, int tid, uint32_t* x) {
 #pragma unroll
@@ -398,9 +413,63 @@ __device__ __forceinline__ void w_words_global(const Params& p, bool fwd, int tc
       n = kb * BK + nl;
       off = static_cast<int64_t>(tcol) * (BN / 4) + 24 * static_cast<int64_t>(rank) + 4 * j;
     }
-    x[i] = (n < p.N && off < p.kb_bytes)
-               ? __ldg(reinterpret_cast<const uint32_t*>(p.wp + n * p.kb_bytes + off))
-               : 0u;
+    uint32_t w = 0u;
+    if (n < p.N && off < p.kb_bytes) {
+      const uint8_t* src = p.wp + n * p.kb_bytes + off;
+      if (kWords4 || p.w_vec4) {
+        w = __ldg(reinterpret_cast<const uint32_t*>(src));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (off + j < p.kb_bytes) w |= static_cast<uint32_t>(__ldg(src + j)) << (8 * j);
+      }
+    }
+    x[i] = w;
+  }
+}
+
+// The 64 activation bytes of thread half h (reduction elements
+// [kb * BK + 64 h, +64)) of row m, from global memory; 0 past the rows or the
+// reduction (as TMA's zero fill).
+__device__ __forceinline__ void act_words_global(const Params& p, int64_t m, int64_t kb, int h,
+                                                 uint32_t (&x)[16]) {
+  const int64_t k0 = kb * BK + 64 * h;
+  const int8_t* rowp = p.act + m * p.act_cols;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int64_t k = k0 + 4 * i;
+    uint32_t w = 0u;
+    if (m < p.act_rows && k < p.act_cols) {
+      if (p.act_vec4 && k + 4 <= p.act_cols) {
+        w = __ldg(reinterpret_cast<const uint32_t*>(rowp + k));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (k + j < p.act_cols)
+            w |= static_cast<uint32_t>(static_cast<uint8_t>(__ldg(rowp + k + j))) << (8 * j);
+      }
+    }
+    x[i] = w;
+  }
+}
+
+// act_load's conversion, from words already in registers (x[4 c + j] holds
+// elements 64 h + 16 c + 4 j .. +3).
+template <bool kEvenOdd>
+__device__ __forceinline__ void act_conv(const uint32_t (&x)[16], uint32_t (&v)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if (kEvenOdd) {
+      s8x4_to_f16_evenodd(x[4 * c], v[8 * c + 0], v[8 * c + 4]);
+      s8x4_to_f16_evenodd(x[4 * c + 1], v[8 * c + 1], v[8 * c + 5]);
+      s8x4_to_f16_evenodd(x[4 * c + 2], v[8 * c + 2], v[8 * c + 6]);
+      s8x4_to_f16_evenodd(x[4 * c + 3], v[8 * c + 3], v[8 * c + 7]);
+    } else {
+      tc::s8x4_to_f16(x[4 * c], v[8 * c + 0], v[8 * c + 1]);
+      tc::s8x4_to_f16(x[4 * c + 1], v[8 * c + 2], v[8 * c + 3]);
+      tc::s8x4_to_f16(x[4 * c + 2], v[8 * c + 4], v[8 * c + 5]);
+      tc::s8x4_to_f16(x[4 * c + 3], v[8 * c + 6], v[8 * c + 7]);
+    }
   }
 }
 
@@ -421,7 +490,7 @@ __device__ __forceinline__ void w_dx_store(uint8_t* opb, int tid, const uint32_t
 
 // ------------------------------------------------------------------ kernel
 
-template <int OP, bool kWGlobal>
+template <int OP, int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc2_kernel(const Params p, const __grid_constant__ CUtensorMap map_a,
                const __grid_constant__ CUtensorMap map_w,
@@ -456,7 +525,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < RAW_STAGES; ++s) {
       mbar_init(&raw_full[s], 1);
       // without weight TMA only the activation warps read the raw stages
-      mbar_init(&raw_empty[s], kWGlobal ? kActWarps : kConvWarps);
+      // the warps that read the raw stages release them
+      const int readers = (p.a_tma ? kActWarps : 0) + (p.w_tma ? kWWarps : 0);
+      mbar_init(&raw_empty[s], kMode == kModeTma ? kConvWarps
+                               : kMode == kModeWGlobal ? kActWarps
+                               : (readers > 0 ? readers : 1));
     }
     for (int s = 0; s < OP_STAGES; ++s) {
       mbar_init(&op_full[s], kConvWarps + 1);  // own converters + the odd CTA's forwarder
@@ -493,17 +566,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     static_assert(kFwdWordsPerThread == 3 && kDxWordsPerThread == 3, "three words per thread");
     // weights from global memory: this stage's words, loaded during the
     // previous stage (while that one waited for its operand slot)
-    // kWGlobal: the instantiation for Wp rows without weight TMA (p.w_tma == 0)
-    const bool w_global = kWGlobal && !act_warp;
+    const bool wg = kMode == kModeWGlobal || (kMode == kModeAGlobal && !p.w_tma);
+    const bool w_global = wg && !act_warp;
+    const bool a_global = kMode == kModeAGlobal && act_warp && !p.a_tma;
+    uint32_t ax[16];  // a_global: this stage's activation words, loaded a stage ahead
+    if (a_global && pair < num_tiles)
+      act_words_global(p, static_cast<int64_t>(pair / p.tiles_c) * BMP + rank * 128 + row, 0, h, ax);
     uint32_t wx[3] = {0u, 0u, 0u};
-    if (kWGlobal && w_global && pair < num_tiles)
-      w_words_global(p, OP == kOpFwd, pair % p.tiles_c, 0, rank, wtid, wx);
+    if (w_global && pair < num_tiles)
+      w_words_global<kMode == kModeWGlobal>(p, OP == kOpFwd, pair % p.tiles_c, 0, rank, wtid, wx);
     for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
       for (int64_t kb = 0; kb < p.num_stages; ++kb) {
         const uint8_t* ra = raw + rs * L::raw_stage;
         const uint32_t act_taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kActCol +
                                    os * (BK / 2) + 32 * h;
-        if (kWGlobal && w_global) {
+        if (kMode == kModeAGlobal && a_global) {
+          uint32_t v[32];
+          act_conv<OP == kOpFwd>(ax, v);
+          // the next stage's words go in flight now
+          const bool last_kb = kb + 1 == p.num_stages;
+          const int ntile = last_kb ? tile + npairs : tile;
+          if (ntile < num_tiles)
+            act_words_global(p, static_cast<int64_t>(ntile / p.tiles_c) * BMP + rank * 128 + row,
+                             last_kb ? 0 : kb + 1, h, ax);
+          ok = mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tmem_st_32x32b_x32(act_taddr, v);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&signal[os]);
+          if (++rs == RAW_STAGES) { rs = 0; rph ^= 1u; }
+          if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
+          continue;
+        }
+        if (kMode != kModeTma && w_global) {
           uint32_t v[32];
 #pragma unroll
           for (int i = 0; i < 3; ++i) decode_word_f16(wx[i], v + 8 * i);
@@ -511,7 +608,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const bool last_kb = kb + 1 == p.num_stages;
           const int ntile = last_kb ? tile + npairs : tile;
           if (ntile < num_tiles)
-            w_words_global(p, OP == kOpFwd, ntile % p.tiles_c, last_kb ? 0 : kb + 1, rank, wtid, wx);
+            w_words_global<kMode == kModeWGlobal>(p, OP == kOpFwd, ntile % p.tiles_c, last_kb ? 0 : kb + 1, rank, wtid, wx);
           ok = mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           if (OP == kOpFwd)
@@ -561,13 +658,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tensormap(&map_a);
-      if (!kWGlobal) prefetch_tensormap(&map_w);
+    const bool wg_p = kMode == kModeWGlobal || (kMode == kModeAGlobal && !p.w_tma);
+    // with both operands from global memory there is nothing to copy
+    const bool ag_p = kMode == kModeAGlobal && !p.a_tma;
+    const bool idle = ag_p && wg_p;
+    if (lane == 0 && !idle) {
+      if (!ag_p) prefetch_tensormap(&map_a);
+      if (!wg_p) prefetch_tensormap(&map_w);
     }
     uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
     bool ok = true;
-    for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+    for (int tile = pair; ok && !idle && tile < num_tiles; tile += npairs) {
       const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
       const int ay = tr * BMP + static_cast<int>(rank) * 128;
       int wx, wy;  // weight box origin and its per-stage step
@@ -585,9 +686,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (lane == 0) {
           uint8_t* dst = raw + stage * L::raw_stage;
-          mbar_arrive_expect_tx(&raw_full[stage], RAW_A + (kWGlobal ? 0 : L::raw_w));
-          tma_load_2d(dst, &map_a, &raw_full[stage], static_cast<int>(kb * BK), ay);
-          if (!kWGlobal) {
+          mbar_arrive_expect_tx(&raw_full[stage], (ag_p ? 0 : RAW_A) + (wg_p ? 0 : L::raw_w));
+          if (!ag_p) tma_load_2d(dst, &map_a, &raw_full[stage], static_cast<int>(kb * BK), ay);
+          if (!wg_p) {
             if (OP == kOpFwd)
               tma_load_2d(dst + RAW_A, &map_w, &raw_full[stage], static_cast<int>(kb * (BK / 4)), wy);
             else

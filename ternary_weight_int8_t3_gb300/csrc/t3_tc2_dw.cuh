@@ -78,8 +78,39 @@ struct Params {
   int64_t num_stages;    // stages along the reduction
   int tiles_r, tiles_c;  // tiles along k, along n
   int num_chunks;        // exact chunks along the reduction
+  // operands a TMA map cannot describe (row stride or base not 16-byte
+  // aligned): the converters load them from global memory (kGlobal)
+  const int8_t* a;       // [M][K]
+  const int8_t* dy;      // [M][N]
+  int a_vec4, dy_vec4;   // rows 4-byte aligned: word loads (else bytes)
+  int32_t* out;          // dW, for per-element adds when it cannot take bulk adds
+  int use_tma_out;
+  int global_ops;        // 1: the kGlobal instantiation
   int* err;
 };
+
+// 16 bytes of row m, columns [col, col + 16), from global memory; 0 past the
+// rows or columns (as TMA's zero fill).
+__device__ __forceinline__ uint4 row16_global(const int8_t* base, int64_t rows, int64_t cols,
+                                              int vec4, int64_t m, int64_t col) {
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  if (m < rows) {
+    const int8_t* rowp = base + m * cols;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t k = col + 4 * i;
+      if (vec4 && k + 4 <= cols) {
+        w[i] = __ldg(reinterpret_cast<const uint32_t*>(rowp + k));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (k + j < cols)
+            w[i] |= static_cast<uint32_t>(static_cast<uint8_t>(__ldg(rowp + k + j))) << (8 * j);
+      }
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 // The (tile, chunk) units of one CTA pair: tile-major numbers [u0, u1).
 struct Units {
@@ -117,35 +148,44 @@ __host__ __device__ constexpr uint32_t idesc_f16_mn(int m, int n) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// One unit of one operand's stage: raw int8 row m (of 64), 16-byte chunk c
+// (16 MN values) -> two 8-value f16 chunks 2c, 2c+1 of MN-major atom c/4.
+// Threads c >= 4 write their odd chunk first so that each 8-thread store
+// phase hits 8 distinct bank groups.
+__device__ __forceinline__ void widen_unit(uint4 x, int m, int c, uint8_t* op) {
+  uint4 lo, hi;
+  tc::s8x4_to_f16(x.x, lo.x, lo.y);
+  tc::s8x4_to_f16(x.y, lo.z, lo.w);
+  tc::s8x4_to_f16(x.z, hi.x, hi.y);
+  tc::s8x4_to_f16(x.w, hi.z, hi.w);
+  const int r = m & 7;
+  uint8_t* row = op + (m >> 3) * K_GROUP + (c >> 2) * MN_ATOM + r * 128;
+  // selects, not a branch: a branch on c would split every warp and issue
+  // each store twice with half of the threads
+  const bool odd_first = c >= 4;
+  const int c0 = (2 * c) & 7, c1 = (2 * c + 1) & 7;
+  const int f = odd_first ? c1 : c0, g = odd_first ? c0 : c1;
+  const uint4 first = odd_first ? hi : lo, second = odd_first ? lo : hi;
+  sts128(row + ((f ^ r) << 4), first);
+  sts128(row + ((g ^ r) << 4), second);
+}
+
 // One operand of one stage: raw int8 [64 m][128 MN] -> f16 MN-major atoms.
-// Unit u = (row m, 16-byte raw chunk c): 16 MN values -> two 8-value f16
-// chunks 2c, 2c+1 of atom c/4.  Threads c >= 4 write their odd chunk first so
-// that each 8-thread store phase hits 8 distinct bank groups.
+// Unit u = (row m, 16-byte raw chunk c), two per thread.
 __device__ __forceinline__ void widen_mn(const uint8_t* raw, uint8_t* op, int tid) {
   constexpr int kUnits = BK * 8;
 #pragma unroll
   for (int u = tid; u < kUnits; u += kHalfThreads) {
     const int m = u >> 3, c = u & 7;
-    const uint4 x = *reinterpret_cast<const uint4*>(raw + m * 128 + 16 * c);
-    uint4 lo, hi;
-    tc::s8x4_to_f16(x.x, lo.x, lo.y);
-    tc::s8x4_to_f16(x.y, lo.z, lo.w);
-    tc::s8x4_to_f16(x.z, hi.x, hi.y);
-    tc::s8x4_to_f16(x.w, hi.z, hi.w);
-    const int r = m & 7;
-    uint8_t* row = op + (m >> 3) * K_GROUP + (c >> 2) * MN_ATOM + r * 128;
-    // selects, not a branch: a branch on c would split every warp and issue
-    // each store twice with half of the threads
-    const bool odd_first = c >= 4;
-    const int c0 = (2 * c) & 7, c1 = (2 * c + 1) & 7;
-    const int f = odd_first ? c1 : c0, g = odd_first ? c0 : c1;
-    const uint4 first = odd_first ? hi : lo, second = odd_first ? lo : hi;
-    sts128(row + ((f ^ r) << 4), first);
-    sts128(row + ((g ^ r) << 4), second);
+    widen_unit(*reinterpret_cast<const uint4*>(raw + m * 128 + 16 * c), m, c, op);
   }
 }
+constexpr int kUnitsPerThread = BK * 8 / kHalfThreads;
+static_assert(kUnitsPerThread == 2, "two units per converter thread");
 
-template <int CHUNK>
+// kGlobal: the instantiation whose converters load the operands from global
+// memory (no raw stages, an idle producer).
+template <int CHUNK, bool kGlobal>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     dw2_kernel(const Params p, const __grid_constant__ CUtensorMap map_a,
                const __grid_constant__ CUtensorMap map_dy,
@@ -215,6 +255,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!units.has(tile, c)) continue;
       const int64_t k1 = min(p.num_stages, (c + 1) * kChunkStages);
       for (int64_t kb = c * kChunkStages; kb < k1; ++kb) {
+        if (kGlobal) {
+          // this stage's two units go in flight before the wait for the slot
+          const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
+          uint4 x[kUnitsPerThread];
+#pragma unroll
+          for (int i = 0; i < kUnitsPerThread; ++i) {
+            const int u = htid + i * kHalfThreads, m = u >> 3, cc = u & 7;
+            const int64_t mg = kb * BK + m;
+            x[i] = a_warp ? row16_global(p.a, p.M, p.K, p.a_vec4, mg,
+                                         static_cast<int64_t>(tr) * BMP + rank * 128 + 16 * cc)
+                          : row16_global(p.dy, p.M, p.N, p.dy_vec4, mg,
+                                         static_cast<int64_t>(tcol) * BN + rank * BNH + 16 * cc);
+          }
+          ok = mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          uint8_t* o = op + os * OP_STAGE + (a_warp ? 0 : OP_OPERAND);
+#pragma unroll
+          for (int i = 0; i < kUnitsPerThread; ++i) {
+            const int u = htid + i * kHalfThreads;
+            widen_unit(x[i], u >> 3, u & 7, o);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&signal[os]);
+          if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
+          continue;
+        }
         ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2) &&
              mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -233,13 +300,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && !kGlobal) {
       prefetch_tensormap(&map_a);
       prefetch_tensormap(&map_dy);
     }
     uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
     bool ok = true;
-    for (int c = 0; ok && c < units.nc; ++c)
+    for (int c = 0; ok && !kGlobal && c < units.nc; ++c)
     for (int tile = units.t0; ok && tile <= units.t1; ++tile) {
       if (!units.has(tile, c)) continue;
       const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
@@ -348,7 +415,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t acc_empty_leader0 = tc2::peer_addr(&acc_empty[0], 0);
     uint32_t ab = 0, aph = 0, slab = 0;
     bool ok = true;
-    if (epi_tid == 0) prefetch_tensormap(&map_out);
+    if (epi_tid == 0 && p.use_tma_out) prefetch_tensormap(&map_out);
     // every unit adds onto the output: the zeroing grid must have completed
     grid_dependency_wait();
     for (int c = 0; ok && c < units.nc; ++c)
@@ -368,6 +435,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * BN + cb * 32,
                              v);
           tmem_wait_ld();
+          if (!p.use_tma_out) {
+            // rows of dW not 16-byte aligned: one atomic add per element
+            const int64_t row = static_cast<int64_t>(row0) + srow;
+            if (row < p.K) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (col0 + e < p.N) atomicAdd(p.out + row * p.N + col0 + e, tc::f32_bits_to_i32(v[e]));
+            }
+            continue;
+          }
           uint8_t* buf = stage_out + (slab & 1) * STAGE_OUT;
           if (epi_tid == 0) bulk_wait_group_read<1>();
           named_bar_sync(kEpiBarrier, 128);
@@ -393,7 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (++ab == ACC_BUFS) { ab = 0; aph ^= 1u; }
       }
     }
-    if (epi_tid == 0) bulk_wait_group<0>();
+    if (epi_tid == 0 && p.use_tma_out) bulk_wait_group<0>();
   }
 
   tc_fence_before();

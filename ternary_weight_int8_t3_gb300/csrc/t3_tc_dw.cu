@@ -29,7 +29,10 @@ int launch_dw2(const dw2::Params& p, const CUtensorMap& ma, const CUtensorMap& m
   static std::atomic<bool> attr_done[64];
   if (dev < 0 || dev >= 64) return T3_EDEVICE;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(dw2::dw2_kernel<dw2::kChunkElems>,
+    if (cudaFuncSetAttribute(dw2::dw2_kernel<dw2::kChunkElems, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dw2::SMEM_ALLOC) != cudaSuccess ||
+        cudaFuncSetAttribute(dw2::dw2_kernel<dw2::kChunkElems, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              dw2::SMEM_ALLOC) != cudaSuccess)
       return T3_ECUDA;
@@ -45,8 +48,11 @@ int launch_dw2(const dw2::Params& p, const CUtensorMap& ma, const CUtensorMap& m
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, dw2::dw2_kernel<dw2::kChunkElems>, p, ma, mdy, mo) != cudaSuccess)
-    return T3_ECUDA;
+  const cudaError_t le =
+      p.global_ops ? cudaLaunchKernelEx(&cfg, dw2::dw2_kernel<dw2::kChunkElems, true>, p, ma, mdy, mo)
+                   : cudaLaunchKernelEx(&cfg, dw2::dw2_kernel<dw2::kChunkElems, false>, p, ma, mdy,
+                                        mo);
+  if (le != cudaSuccess) return T3_ECUDA;
   return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
 }
 

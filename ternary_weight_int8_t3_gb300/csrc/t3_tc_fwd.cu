@@ -30,17 +30,21 @@ int launch_tc2_fwd(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMa
   static std::atomic<bool> attr_done[64];
   if (dev < 0 || dev >= 64) return T3_EDEVICE;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(tc2::tc2_kernel<kOpFwd, false>,
+    if (cudaFuncSetAttribute(tc2::tc2_kernel<kOpFwd, tc2::kModeTma>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(tc2::tc2_kernel<kOpFwd, true>,
+        cudaFuncSetAttribute(tc2::tc2_kernel<kOpFwd, tc2::kModeWGlobal>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(tc2::tc2_kernel<kOpFwd, tc2::kModeAGlobal>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
       return T3_ECUDA;
     attr_done[dev].store(true, std::memory_order_release);
   }
-  if (p.w_tma)
-    tc2::tc2_kernel<kOpFwd, false><<<grid, tc2::kThreads, kSmem, s>>>(p, ma, mw, mo);
+  if (p.mode == tc2::kModeTma)
+    tc2::tc2_kernel<kOpFwd, tc2::kModeTma><<<grid, tc2::kThreads, kSmem, s>>>(p, ma, mw, mo);
+  else if (p.mode == tc2::kModeWGlobal)
+    tc2::tc2_kernel<kOpFwd, tc2::kModeWGlobal><<<grid, tc2::kThreads, kSmem, s>>>(p, ma, mw, mo);
   else
-    tc2::tc2_kernel<kOpFwd, true><<<grid, tc2::kThreads, kSmem, s>>>(p, ma, mw, mo);
+    tc2::tc2_kernel<kOpFwd, tc2::kModeAGlobal><<<grid, tc2::kThreads, kSmem, s>>>(p, ma, mw, mo);
   return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
 }
 

@@ -316,3 +316,31 @@ def test_weight_rows_not_16_byte_aligned(M, N, K):
     wp = oracle.pack(t3_synth.ternary(g, (K, N)))
     np.testing.assert_array_equal(run_fwd(A, wp), oracle.fwd(A, wp))
     np.testing.assert_array_equal(run_dx(dY, wp, K), oracle.dx(dY, wp, K))
+
+
+@pytest.mark.parametrize("M,N,K", [(1782, 729, 243), (300, 243, 729), (257, 1001, 999), (64, 17, 33)])
+def test_rows_not_16_byte_aligned(M, N, K):
+    # activation and weight rows TMA cannot address: the pair pipeline's
+    # converters load them from global memory (words or single bytes)
+    g = t3_synth.rng(3 * M + N + K)
+    A = t3_synth.int8_uniform(g, (M, K))
+    dY = t3_synth.int8_uniform(g, (M, N))
+    wp = oracle.pack(t3_synth.ternary(g, (K, N)))
+    np.testing.assert_array_equal(run_fwd(A, wp), oracle.fwd(A, wp))
+    np.testing.assert_array_equal(run_dx(dY, wp, K), oracle.dx(dY, wp, K))
+    # dW: operands loaded by its converters; N % 4 != 0 adds element by element
+    np.testing.assert_array_equal(run_dw(A, dY), oracle.dw(A, dY))
+
+
+def test_unaligned_large_sampled_rows():
+    M, N, K = 4096, 4096, 4088
+    g = t3_synth.rng(4088)
+    A = t3_synth.int8_uniform(g, (M, K))
+    dY = t3_synth.int8_uniform(g, (M, 4088))
+    wp = oracle.pack(t3_synth.ternary(g, (K, N)))
+    rows = np.array([0, 1, 255, 256, 2047, 4095])
+    np.testing.assert_array_equal(run_fwd(A, wp)[rows], oracle.fwd(A, wp, rows))
+    wp2 = oracle.pack(t3_synth.ternary(g, (K, 4088)))
+    np.testing.assert_array_equal(run_dx(dY, wp2, K)[rows], oracle.dx(dY, wp2, K, rows))
+    krows = np.array([0, 127, 128, 2047, 4087])
+    np.testing.assert_array_equal(run_dw(A, dY)[krows], oracle.dw(A, dY, krows))
