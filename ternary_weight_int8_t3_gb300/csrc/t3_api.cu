@@ -135,51 +135,11 @@ int device_info(const DeviceInfo** out) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-template <int OP>
-int run_tc(const uint8_t* a_src, int64_t a_rows, int64_t a_cols, const uint8_t* b_src,
-           int64_t b_rows, int64_t b_cols, int32_t* out, int64_t out_rows, int64_t out_cols,
-           int64_t reduction, int64_t chunk_kb, cudaStream_t stream) {
-  const DeviceInfo* dev = nullptr;
-  int st = device_info(&dev);
-  if (st != T3_OK) return st;
-  using R = tc::Raw<OP>;
-  tc::Params p{};
-  p.a_src = a_src;
-  p.a_ld = a_cols;
-  p.a_rows = a_rows;
-  p.a_cols = a_cols;
-  p.b_src = b_src;
-  p.b_ld = b_cols;
-  p.b_rows = b_rows;
-  p.b_cols = b_cols;
-  p.out = out;
-  p.out_rows = out_rows;
-  p.out_cols = out_cols;
-  p.num_kb = ceil_div(reduction, tc::BK);
-  p.chunk_kb = chunk_kb;
-  const int64_t tiles_r = ceil_div(out_rows, tc::BM), tiles_c = ceil_div(out_cols, tc::BN);
-  if (tiles_r * tiles_c > kMaxDim) return T3_EINVAL;
-  p.tiles_r = static_cast<int>(tiles_r);
-  p.tiles_c = static_cast<int>(tiles_c);
-  p.err = dev->err_word;
-  p.op_code = OP;
-  CUtensorMap ma, mb, mo;
-  p.use_tma_a = make_u8_map_tiled(&ma, a_src, a_rows, a_cols, a_cols, R::a_rows, R::a_cols) ? 1 : 0;
-  p.use_tma_b = make_u8_map_tiled(&mb, b_src, b_rows, b_cols, b_cols, R::b_rows, R::b_cols) ? 1 : 0;
-  p.use_tma_out = make_i32_map_tiled(&mo, out, out_rows, out_cols, tc::BM, 32, true) ? 1 : 0;
-  const int64_t tiles = tiles_r * tiles_c;
-  const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
-  if (OP == kOpFwd) return launch_tc_fwd(p, ma, mb, mo, grid, stream);
-  if (OP == kOpDx) return launch_tc_dx(p, ma, mb, mo, grid, stream);
-  return launch_tc_dw(p, ma, mb, mo, grid, stream);
-}
-
 // The CTA-pair pipeline for the forward (OP = kOpFwd: act = A [M][K], weights
-// packed along K) or dX (act = dY [M][N], reduction N).  Returns T3_EINVAL
-// without launching when an operand cannot be a TMA source or the output
-// cannot take bulk stores; the caller then uses the single-CTA pipeline (or,
-// for a scaled output kind, the exact int32 product and t3_dequant_i32).  A
-// scaled kind needs the reduction in one exact chunk.
+// packed along K) or dX (act = dY [M][N], reduction N), for operands of any
+// alignment.  A scaled output kind needs bulk stores and the reduction in one
+// exact chunk: otherwise it returns T3_EINVAL without launching, and the
+// caller computes the exact int32 product and then t3_dequant_i32.
 template <int OP>
 int run_tc2(const int8_t* act, const uint8_t* Wp, void* out, int64_t M, int64_t N, int64_t K,
             cudaStream_t stream, int out_kind = tc2::kOutI32, const float* row_scale = nullptr,
@@ -239,8 +199,7 @@ int run_tc2(const int8_t* act, const uint8_t* Wp, void* out, int64_t M, int64_t 
                         : launch_tc2_dx(p, ma, mw, mo, grid, stream);
 }
 
-// The CTA-pair dW pipeline.  Returns T3_EINVAL without launching when A, dY or
-// dW cannot be used with TMA; the caller then uses the single-CTA pipeline.
+// The CTA-pair dW pipeline, for operands and output of any alignment.
 int run_dw2(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N, int64_t K,
             cudaStream_t stream) {
   const DeviceInfo* dev = nullptr;
@@ -353,17 +312,13 @@ int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64
   if (K == 0) return zero_fill(C, M, N, stream);
   if (!A || !Wp || !C) return T3_EINVAL;
   if (K > kMaxTernaryReduction) return T3_EOVERFLOW;
-  const int64_t KB = (K + 3) / 4;
   if (M <= kSmallM) {
     const DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st != T3_OK) return st;
     return launch_skinny_fwd(A, Wp, C, M, N, K, dev->sms, dev->err_word, stream);
   }
-  const int st2 = run_tc2<kOpFwd>(A, Wp, C, M, N, K, stream);
-  if (st2 != T3_EINVAL) return st2;
-  return run_tc<kOpFwd>(reinterpret_cast<const uint8_t*>(A), M, K, Wp, N, KB, C, M, N, K,
-                        tc::kChunkKbTernary, stream);
+  return run_tc2<kOpFwd>(A, Wp, C, M, N, K, stream);
 }
 
 int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, int64_t N,
@@ -373,11 +328,7 @@ int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, 
   if (N == 0) return zero_fill(dX, M, K, stream);
   if (!dY || !Wp || !dX) return T3_EINVAL;
   if (N > kMaxTernaryReduction) return T3_EOVERFLOW;
-  const int64_t KB = (K + 3) / 4;
-  const int st2 = run_tc2<kOpDx>(dY, Wp, dX, M, N, K, stream);
-  if (st2 != T3_EINVAL) return st2;
-  return run_tc<kOpDx>(reinterpret_cast<const uint8_t*>(dY), M, N, Wp, N, KB, dX, M, K, N,
-                       tc::kChunkKbTernary, stream);
+  return run_tc2<kOpDx>(dY, Wp, dX, M, N, K, stream);
 }
 
 int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N,
@@ -387,11 +338,7 @@ int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, in
   if (M == 0) return zero_fill(dW, K, N, stream);
   if (!A || !dY || !dW) return T3_EINVAL;
   if (M > kMaxInt8Reduction) return T3_EOVERFLOW;
-  const int st2 = run_dw2(A, dY, dW, M, N, K, stream);
-  if (st2 != T3_EINVAL) return st2;
-  return run_tc<kOpDw>(reinterpret_cast<const uint8_t*>(A), M, K,
-                       reinterpret_cast<const uint8_t*>(dY), M, N, dW, K, N, M,
-                       tc::kChunkKbInt8, stream);
+  return run_dw2(A, dY, dW, M, N, K, stream);
 }
 
 int t3_pack_ternary_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N,

@@ -3,19 +3,11 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
-#include "t3_tc_gemm.cuh"
+#include "t3_common.cuh"
 #include "t3_tc2.cuh"
 #include "t3_tc2_dw.cuh"
 
 namespace t3 {
-
-// Launch the tensor-core pipeline for one product.  Returns a t3_status.
-int launch_tc_fwd(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap& mb,
-                  const CUtensorMap& mo, int grid, cudaStream_t s);
-int launch_tc_dx(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap& mb,
-                  const CUtensorMap& mo, int grid, cudaStream_t s);
-int launch_tc_dw(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap& mb,
-                  const CUtensorMap& mo, int grid, cudaStream_t s);
 
 // Tensor maps for 2-D row-major matrices (row stride = cols elements).  They
 // return false, leaving *map zeroed, when TMA cannot be used (base or row

@@ -35,7 +35,7 @@
 #include <cstdint>
 
 #include "t3.h"
-#include "t3_tc_gemm.cuh"
+#include "t3_common.cuh"
 
 namespace t3 {
 namespace tc2 {

@@ -1,26 +1,9 @@
-// t3_tc_dw.cu -- instantiates the tensor-core pipeline for one product.
+// t3_tc_dw.cu -- instantiates and launches the pair pipeline for one product.
 #include <atomic>
 #include "t3_internal.h"
 #include "t3.h"
 
 namespace t3 {
-
-int launch_tc_dw(const tc::Params& p, const CUtensorMap& ma, const CUtensorMap& mb,
-                  const CUtensorMap& mo, int grid, cudaStream_t s) {
-  constexpr int kSmem = tc::Layout<kOpDw>::smem_alloc;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
-  static std::atomic<bool> attr_done[64];
-  if (dev < 0 || dev >= 64) return T3_EDEVICE;
-  if (!attr_done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(tc::tc_gemm_kernel<kOpDw>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmem) != cudaSuccess)
-      return T3_ECUDA;
-    attr_done[dev].store(true, std::memory_order_release);
-  }
-  tc::tc_gemm_kernel<kOpDw><<<grid, tc::kThreads, kSmem, s>>>(p, ma, mb, mo);
-  return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
-}
 
 int launch_dw2(const dw2::Params& p, const CUtensorMap& ma, const CUtensorMap& mdy,
                const CUtensorMap& mo, int grid, cudaStream_t s) {

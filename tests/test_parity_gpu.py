@@ -142,8 +142,9 @@ def test_raw_codes_and_pad_bits():
         assert_same(run_dx(dY, wp, K), oracle.dx(dY, wp, K), f"dX raw {M}x{N}x{K}")
 
 
-def test_unaligned_pointers_take_plain_load_path():
-    """Operands at odd byte offsets cannot be TMA sources; results are the same."""
+def test_unaligned_pointers_take_global_load_modes():
+    """Operands at odd byte offsets cannot be TMA sources: the converters load
+    them from global memory (single bytes); results are the same."""
     M, N, K = 150, 200, 320
     A, w, dY = inputs(M, N, K, seed=99)
     wp = t3.t3_pack_ternary(w)
