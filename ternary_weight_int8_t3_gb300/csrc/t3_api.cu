@@ -97,6 +97,11 @@ constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = 2147483647LL;           // TMA coordinates are int32
 constexpr int64_t kMaxTernaryReduction = 16777215;  // 128 * K <= INT32_MAX
 constexpr int64_t kMaxInt8Reduction = 131071;       // 16384 * M <= INT32_MAX
+// What splitting a pair pipeline's last wave costs, in stages of one pair
+// (~0.7 us each): the zeroing grid and the dependent launch before the
+// product and each pair's last partial tile added rather than stored (~5 us
+// per call), and ~5 % more time per stage in the split kernel (measured).
+constexpr int64_t kSplitCostStages = 8;
 constexpr int64_t kSmallM = 32;                     // forward rows served by the small-M path
 
 struct DeviceInfo {
@@ -193,7 +198,34 @@ int run_tc2(const int8_t* act, const uint8_t* Wp, void* out, int64_t M, int64_t 
            : (a_ok && p.w_vec4) ? tc2::kModeWGlobal
                                 : tc2::kModeAGlobal;
   p.err = dev->err_word;
-  const int64_t pairs = std::min<int64_t>(tiles_r * tiles_c, dev->sms / 2);
+  // Schedule.  Whole tiles dealt round-robin keep the busiest pair busy for
+  // ceil(T / P) tiles of S stages.  Dealing only the full waves that way and
+  // splitting the stages of the remaining tiles evenly over all pairs
+  // (stream-K) takes floor(T / P) tiles plus ceil(rem * S / P) stages, and
+  // costs the zeroing of those tiles' rows and one more partial-tile flush
+  // per pair, counted as kSplitCostStages.  A scaled epilogue needs a tile's
+  // whole sum, so it keeps whole tiles, and so do the global-load modes.
+  const int64_t num_tiles = tiles_r * tiles_c;
+  const int64_t max_pairs = std::max(dev->sms / 2, 1);
+  const int64_t waves = num_tiles / max_pairs, rem = num_tiles % max_pairs;
+  int64_t dp_tiles = num_tiles;
+  if (out_kind == tc2::kOutI32 && p.mode == tc2::kModeTma && rem != 0) {
+    const int64_t t_whole = (waves + 1) * p.num_stages;
+    const int64_t t_split =
+        (waves * p.num_stages + ceil_div(rem * p.num_stages, max_pairs)) * 21 / 20 +
+        kSplitCostStages;
+    if (t_split < t_whole) dp_tiles = waves * max_pairs;
+  }
+  p.dp_tiles = static_cast<int>(dp_tiles);
+  const bool split = dp_tiles < num_tiles;
+  if (split) {
+    // from the first tile row that holds a split tile to the end
+    const int64_t row0 = (dp_tiles / tiles_c) * tc2::BMP;
+    st = launch_zero_pdl(static_cast<int32_t*>(out) + row0 * out_cols, (M - row0) * out_cols,
+                         dev->sms, stream);
+    if (st != T3_OK) return st;
+  }
+  const int64_t pairs = split ? max_pairs : std::min(num_tiles, max_pairs);
   const int grid = static_cast<int>(2 * pairs);
   return (OP == kOpFwd) ? launch_tc2_fwd(p, ma, mw, mo, grid, stream)
                         : launch_tc2_dx(p, ma, mw, mo, grid, stream);

@@ -103,5 +103,13 @@ __device__ __forceinline__ void store_row32(int32_t* dst, const uint32_t (&v)[32
   }
 }
 
+// Adds a row of up to 32 exact sums (f32 bit patterns) into int32 output
+// elements that other CTAs also add into.
+__device__ __forceinline__ void atomic_add_row32(int32_t* dst, const uint32_t (&v)[32], int valid) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i < valid) atomicAdd(dst + i, f32_bits_to_i32(v[i]));
+}
+
 }  // namespace tc
 }  // namespace t3

@@ -17,7 +17,9 @@ bool make_u8_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_t
 bool make_i32_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
                         int box_rows, int box_cols, bool swizzle128);
 
-// CTA-pair pipeline for the forward and dX products (all operands TMA-able).
+// CTA-pair pipeline for the forward and dX products.  With a split schedule
+// (p.dp_tiles below the tile count) the rows the stream-K pieces add into must
+// have been zeroed by launch_zero_pdl just before on `s`.
 int launch_tc2_fwd(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap& mw,
                    const CUtensorMap& mo, int grid, cudaStream_t s);
 int launch_tc2_dx(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap& mw,

@@ -111,8 +111,54 @@ struct Params {
   int act_vec4;           // activation rows 4-byte aligned: word loads (else bytes)
   int a_tma;              // 1: activations come by TMA
   int mode;               // kernel instantiation: kModeTma, kModeWGlobal, kModeAGlobal
+  // Schedule: tiles [0, dp_tiles) are taken whole, round-robin over the
+  // pairs; the (tile, stage) iterations of the remaining tiles are split into
+  // equal contiguous ranges, one per pair (stream-K).  Those pieces add their
+  // int32 sums onto output rows that a chained grid has zeroed; when
+  // dp_tiles < tiles_r * tiles_c every output write waits for that grid.
+  int dp_tiles;
   int* err;
 };
+
+// One piece of a pair's work: a tile and the range [kb0, kb1) of its
+// reduction stages.  Every role of both CTAs walks the same pieces in the same
+// order, so their stage rings stay in step.
+struct Piece {
+  int tile, kb0, kb1;
+};
+
+// Piece i (0, 1, ...) of a pair: first the whole tiles pair, pair + npairs, ...
+// below dp_tiles, then the pair's equal share of the remaining tiles'
+// (tile, stage) iterations, cut at tile boundaries.  False past the last one.
+// 32-bit indices suffice: a reduction has at most 131072 stages and the split
+// part fewer than npairs tiles.
+__device__ __forceinline__ bool get_piece(const Params& p, int pair, int npairs, int i, Piece& w) {
+  const int S = static_cast<int>(p.num_stages);
+  const int whole = pair < p.dp_tiles ? (p.dp_tiles - 1 - pair) / npairs + 1 : 0;
+  if (i < whole) {
+    w.tile = pair + i * npairs;
+    w.kb0 = 0;
+    w.kb1 = S;
+    return true;
+  }
+  const int64_t total = static_cast<int64_t>(p.tiles_r * p.tiles_c - p.dp_tiles) * S;
+  const int b = static_cast<int>(total * pair / npairs);
+  const int e = static_cast<int>(total * (pair + 1) / npairs);
+  const int t = b / S + (i - whole);  // split tile, counted from dp_tiles
+  const int s0 = t * S > b ? t * S : b;
+  if (s0 >= e) return false;
+  w.tile = p.dp_tiles + t;
+  w.kb0 = s0 - t * S;
+  w.kb1 = (e - t * S < S) ? e - t * S : S;
+  return true;
+}
+
+// End of the exact accumulation group that starts at stage c0 of a piece
+// ending at kb1: groups never cross a multiple of kChunkStages.
+__device__ __forceinline__ int chunk_end(int c0, int kb1) {
+  const int e = (c0 / static_cast<int>(kChunkStages) + 1) * static_cast<int>(kChunkStages);
+  return e < kb1 ? e : kb1;
+}
 
 // Kernel instantiations: all operands by TMA; weights from global memory as
 // whole words (activations by TMA); and the general one, where each operand
@@ -488,13 +534,23 @@ __device__ __forceinline__ void w_dx_store(uint8_t* opb, int tid, const uint32_t
   }
 }
 
+// How many stages one pair runs in all (whole tiles and stream-K pieces).
+__device__ __forceinline__ int64_t pair_stage_count(const Params& p, int pair, int npairs) {
+  const int64_t whole = pair < p.dp_tiles ? (p.dp_tiles - 1 - pair) / npairs + 1 : 0;
+  const int64_t total = static_cast<int64_t>(p.tiles_r * p.tiles_c - p.dp_tiles) * p.num_stages;
+  return whole * p.num_stages + total * (pair + 1) / npairs - total * pair / npairs;
+}
+
 // ------------------------------------------------------------------ kernel
 
-template <int OP, int kMode>
+// kSplit: the split schedule (operands by TMA only); without it every pair
+// takes whole tiles and the loops below reduce to plain tile loops.
+template <int OP, int kMode, bool kSplit>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc2_kernel(const Params p, const __grid_constant__ CUtensorMap map_a,
                const __grid_constant__ CUtensorMap map_w,
                const __grid_constant__ CUtensorMap map_out) {
+  static_assert(!kSplit || kMode == kModeTma, "the split schedule takes TMA operands");
   using L = Layout<OP>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base_addr = smem_addr(smem_raw);
@@ -575,8 +631,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t wx[3] = {0u, 0u, 0u};
     if (w_global && pair < num_tiles)
       w_words_global<kMode == kModeWGlobal>(p, OP == kOpFwd, pair % p.tiles_c, 0, rank, wtid, wx);
-    for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
-      for (int64_t kb = 0; kb < p.num_stages; ++kb) {
+    // the split schedule only needs the count of the pair's stages here
+    int64_t left = kSplit ? pair_stage_count(p, pair, npairs) : 0;
+    for (int tile = pair; ok && tile < (kSplit ? pair + 1 : num_tiles); tile += npairs) {
+      for (int64_t kb = 0; kSplit ? left-- > 0 : kb < p.num_stages; ++kb) {
         const uint8_t* ra = raw + rs * L::raw_stage;
         const uint32_t act_taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kActCol +
                                    os * (BK / 2) + 32 * h;
@@ -668,7 +726,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
     bool ok = true;
-    for (int tile = pair; ok && !idle && tile < num_tiles; tile += npairs) {
+    Piece w{pair, 0, 0};
+    for (int i = 0, tile = pair; ok && !idle; ++i, tile += npairs) {
+      int64_t kb0 = 0, kb1 = p.num_stages;
+      if constexpr (kSplit) {
+        if (!get_piece(p, pair, npairs, i, w)) break;
+        tile = w.tile;
+        kb0 = w.kb0;
+        kb1 = w.kb1;
+      } else {
+        if (tile >= num_tiles) break;
+      }
       const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
       const int ay = tr * BMP + static_cast<int>(rank) * 128;
       int wx, wy;  // weight box origin and its per-stage step
@@ -679,7 +747,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         wx = tcol * (BN / 4);
         wy = 0;
       }
-      for (int64_t kb = 0; kb < p.num_stages; ++kb) {
+      for (int64_t kb = kb0; kb < kb1; ++kb) {
         if (lane == 0)
           ok = mbar_wait(&raw_empty[stage], phase ^ 1u, abort_flag, p.err, code_base | 1);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -716,9 +784,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_f16_f32(BMP, BN) | (OP == kOpDx ? (1u << 16) : 0u);
       uint32_t os = 0, oph = 0, ab = 0, aph = 0;
       bool ok = true, issued_any = false;
-      for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
-        for (int64_t c0 = 0; ok && c0 < p.num_stages; c0 += kChunkStages) {
-          const int64_t c1 = (p.num_stages < c0 + kChunkStages) ? p.num_stages : c0 + kChunkStages;
+      Piece w{pair, 0, 0};
+      for (int i = 0, tile = pair; ok; ++i, tile += npairs) {
+        int64_t kb0 = 0, kb1 = p.num_stages;
+        if constexpr (kSplit) {
+          if (!get_piece(p, pair, npairs, i, w)) break;
+          kb0 = w.kb0;
+          kb1 = w.kb1;
+        } else {
+          if (tile >= num_tiles) break;
+        }
+        for (int64_t c0 = kb0, c1; ok && c0 < kb1; c0 = c1) {
+          c1 = kSplit ? chunk_end(static_cast<int>(c0), static_cast<int>(kb1))
+                      : ((kb1 < c0 + kChunkStages) ? kb1 : c0 + kChunkStages);
           ok = mbar_wait(&acc_empty[ab], aph ^ 1u, abort_flag, p.err, code_base | 3);
           if (!ok) break;
           tc_fence_after();
@@ -763,8 +841,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t op_full_leader0 = peer_addr(&op_full[0], 0);
       uint32_t os = 0, oph = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
-        for (int64_t kb = 0; kb < p.num_stages; ++kb) {
+      Piece w{pair, 0, 0};
+      for (int i = 0, tile = pair; ok; ++i, tile += npairs) {
+        int64_t kb0 = 0, kb1 = p.num_stages;
+        if constexpr (kSplit) {
+          if (!get_piece(p, pair, npairs, i, w)) break;
+          kb0 = w.kb0;
+          kb1 = w.kb1;
+        } else {
+          if (tile >= num_tiles) break;
+        }
+        for (int64_t kb = kb0; kb < kb1; ++kb) {
           ok = mbar_wait(&op_ready[os], oph, abort_flag, p.err, code_base | 5);
           if (!ok) break;
           mbar_arrive_cluster_relaxed(op_full_leader0 + 8u * os);
@@ -783,19 +870,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t ab = 0, aph = 0, slab = 0;
     bool ok = true;
     if (p.use_tma_out && epi_tid == 0) prefetch_tensormap(&map_out);
-    for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+    // split schedule: the zeroing grid launched just before has finished
+    // before the first output write
+    if (kSplit) grid_dependency_wait();
+    Piece w{pair, 0, 0};
+    for (int i = 0, tile = pair; ok; ++i, tile += npairs) {
+      int64_t kb0 = 0, kb1 = p.num_stages;
+      if constexpr (kSplit) {
+        if (!get_piece(p, pair, npairs, i, w)) break;
+        tile = w.tile;
+        kb0 = w.kb0;
+        kb1 = w.kb1;
+      } else {
+        if (tile >= num_tiles) break;
+      }
       const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
       const int row0 = tr * BMP + static_cast<int>(rank) * 128;
       const int64_t row = static_cast<int64_t>(row0) + srow;
       const float rs =
           (p.out_kind != kOutI32 && p.row_scale && row < p.out_rows) ? __ldg(p.row_scale + row) : 1.0f;
-      for (int64_t c0 = 0; c0 < p.num_stages; c0 += kChunkStages) {
+      for (int64_t c0 = kb0, c1; c0 < kb1; c0 = c1) {
+        c1 = kSplit ? chunk_end(static_cast<int>(c0), static_cast<int>(kb1))
+                    : ((kb1 < c0 + kChunkStages) ? kb1 : c0 + kChunkStages);
         ok = mbar_wait(&acc_full[ab], aph, abort_flag, p.err, code_base | 4);
         ok = named_bar_and(kEpiBarrier, 128, __all_sync(0xffffffffu, ok));
         if (!ok) break;
         tc_fence_after();
-        const bool first = (c0 == 0);
-        if (p.use_tma_out && c0 == kChunkStages && epi_tid == 0) bulk_wait_group<0>();
+        // a whole tile's first chunk is stored; its later chunks, and every
+        // stream-K piece, are added
+        const bool sk = kSplit && tile >= p.dp_tiles;
+        const bool first = !sk && c0 == 0;
+        if (p.use_tma_out && !sk && c0 == kChunkStages && epi_tid == 0) bulk_wait_group<0>();
         if (p.out_kind != kOutI32) {
           // the tile's column scales, once (the barrier above ends the previous
           // tile's reads of them)
@@ -848,8 +953,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++slab;
           } else if (row < p.out_rows) {
             const int64_t rem = p.out_cols - col0;
-            tc::store_row32(p.out + row * p.out_cols + col0, v, rem < 32 ? static_cast<int>(rem) : 32,
-                            first, vec_ok);
+            const int valid = rem < 32 ? static_cast<int>(rem) : 32;
+            if (sk)  // other pairs add into the same elements
+              tc::atomic_add_row32(p.out + row * p.out_cols + col0, v, valid);
+            else
+              tc::store_row32(p.out + row * p.out_cols + col0, v, valid, first, vec_ok);
           }
         }
         tc_fence_before();

@@ -345,3 +345,60 @@ def test_unaligned_large_sampled_rows():
     np.testing.assert_array_equal(run_dx(dY, wp2, K)[rows], oracle.dx(dY, wp2, K, rows))
     krows = np.array([0, 127, 128, 2047, 4087])
     np.testing.assert_array_equal(run_dw(A, dY)[krows], oracle.dw(A, dY, krows))
+
+
+# ------------------------------------------------ split (stream-K) schedule --
+# When whole tiles would leave pairs idle for long (few tiles, long
+# reductions), the pair pipeline deals the full waves as whole tiles and
+# splits the remaining tiles' reduction stages evenly over all pairs; those
+# pieces add onto rows zeroed by a chained grid.  The shapes below take that
+# schedule (it needs operands TMA can address), including pieces that cross
+# an exact chunk boundary, outputs that need atomic adds, and a partial wave
+# after a whole one.
+
+@pytest.mark.parametrize("M,N,K", [
+    (300, 400, 4096),    # 6 tiles of 32 stages, all split
+    (40, 20, 70016),     # 1 tile of 547 stages: pieces cross the 65536-element chunk bound
+    (300, 271, 4096),    # output rows not 16-byte aligned: pieces add with atomics
+    (1792, 2112, 2048),  # 77 tiles: one wave whole, 1 tile split, zeroed band shared
+])
+def test_split_schedule_forward(M, N, K):
+    A, w, _ = inputs(M, N, K, seed=M + 3 * N + K)
+    wp = oracle.pack(w)
+    assert_same(run_fwd(A, wp), oracle.fwd(A, wp), f"fwd split {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (300, 4096, 448),    # dX 300x448 over a 4096-long reduction, all split
+    (27, 3456, 1280),    # small M: 7 tiles of 27 stages
+    (40, 70016, 64),     # 547 stages, the chunk bound inside pieces
+    (300, 4096, 447),    # dX rows not 16-byte aligned: atomic adds
+    (1792, 2048, 2112),  # 77 tiles: one wave whole, the rest split
+])
+def test_split_schedule_dx(M, N, K):
+    _, w, dY = inputs(M, N, K, seed=7 * M + N + K)
+    wp = oracle.pack(w)
+    assert_same(run_dx(dY, wp, K), oracle.dx(dY, wp, K), f"dX split {M}x{N}x{K}")
+
+
+def test_split_schedule_chained_calls_see_earlier_outputs():
+    """Split-schedule products back to back on one stream, each reading the
+    previous output's bytes as its input: the zeroing grid of a call must not
+    start before the call before it has finished, nor the product before its
+    inputs exist."""
+    g = t3_synth.rng(23)
+    A0 = t3_synth.int8_uniform(g, (300, 4096))
+    wp0 = oracle.pack(t3_synth.ternary(g, (4096, 400)))
+    wp1 = oracle.pack(t3_synth.ternary(g, (1600, 272)))
+    A2 = t3_synth.int8_uniform(g, (64, 4352))
+    C0 = torch.empty((300, 400), dtype=torch.int32, device="cuda")
+    C1 = torch.empty((300, 272), dtype=torch.int32, device="cuda")
+    C2 = torch.empty((64, 300), dtype=torch.int32, device="cuda")
+    t3.t3_gemm_fwd(_dev(A0), _dev(wp0), K=4096, C=C0)
+    t3.t3_gemm_fwd(C0.view(torch.int8).view(300, 1600), _dev(wp1), K=1600, C=C1)
+    t3.t3_gemm_fwd(_dev(A2), C1.view(torch.uint8).view(300, 1088), K=4352, C=C2)
+    torch.cuda.synchronize()
+    c0, c1, c2 = C0.cpu().numpy(), C1.cpu().numpy(), C2.cpu().numpy()
+    assert_same(c0, oracle.fwd(A0, wp0), "split chained call 1")
+    assert_same(c1, oracle.fwd(c0.view(np.int8).reshape(300, 1600), wp1), "split chained call 2")
+    assert_same(c2, oracle.fwd(A2, c1.view(np.uint8).reshape(300, 1088)), "split chained call 3")
