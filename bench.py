@@ -57,6 +57,9 @@ def parse():
                     help="skip the device-packer sweep (HBM-bound, reported beside the step)")
     ap.add_argument("--no-small-m", action="store_true",
                     help="skip the small-M forward sweep (for launch-list captures)")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the layer step (and its end-to-end form) only: no scaled, "
+                         "quantizer, packer or small-M legs (for launch-list captures)")
     ap.add_argument("--small-m-only", metavar="M,N,K", default=None,
                     help="time one small-M forward configuration of the sweep and exit "
                          "(for profiler captures)")
@@ -570,11 +573,12 @@ def main():
         "clocks": clocks.summary(),
     }
     hbm = peaks.get("hbm_gbs", 6800.0) if peak_src == "measured" else 6800.0
-    line["scaled_f32"] = bench_scaled(t3, torch, dev, stream, A_d, wp_d, dY_d, K)
-    line["quantize_rows"] = bench_quantize(t3, torch, dev, stream, hbm, M, K)
-    if not args.no_pack:
+    if not args.step_only:
+        line["scaled_f32"] = bench_scaled(t3, torch, dev, stream, A_d, wp_d, dY_d, K)
+        line["quantize_rows"] = bench_quantize(t3, torch, dev, stream, hbm, M, K)
+    if not (args.no_pack or args.step_only):
         line["device_pack"] = {"hbm_peak_GBps": hbm, "calls": bench_device_pack(t3, torch, dev, stream, hbm)}
-    if not args.no_small_m:
+    if not (args.no_small_m or args.step_only):
         line["small_m"] = {"hbm_peak_GBps": hbm, "calls": bench_small_m(t3, torch, dev, stream, hbm)}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(A, w, dY)
