@@ -44,7 +44,7 @@ constexpr int BMP = 256;        // dW rows (k) per pair tile, 128 per CTA
 constexpr int BN = 256;         // dW columns (n) per pair tile, 128 per CTA
 constexpr int BNH = BN / 2;
 constexpr int BK = 64;          // reduction elements (m) per stage
-constexpr int RAW_STAGES = 3;
+constexpr int RAW_STAGES = 4;
 constexpr int OP_STAGES = 4;    // converted stages: the converter-to-MMA hand-off is latency-bound
 constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512
