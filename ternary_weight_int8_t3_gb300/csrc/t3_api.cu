@@ -98,9 +98,10 @@ constexpr int64_t kMaxDim = 2147483647LL;           // TMA coordinates are int32
 constexpr int64_t kMaxTernaryReduction = 16777215;  // 128 * K <= INT32_MAX
 constexpr int64_t kMaxInt8Reduction = 131071;       // 16384 * M <= INT32_MAX
 // What splitting a pair pipeline's last wave costs, in stages of one pair
-// (~0.7 us each): the zeroing grid and the dependent launch before the
-// product and each pair's last partial tile added rather than stored (~5 us
-// per call), and ~5 % more time per stage in the split kernel (measured).
+// (~0.7 us each), fitted to measurements: the split kernel runs ~5 % slower
+// per stage than the whole-tile one, and each piece ends in an accumulator
+// flush that adds rather than stores, which short pieces cannot hide.  The
+// zeroing grid and the dependent launch before it cost nothing measurable.
 constexpr int64_t kSplitCostStages = 8;
 constexpr int64_t kSmallM = 32;                     // forward rows served by the small-M path
 
