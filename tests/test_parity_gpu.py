@@ -361,6 +361,7 @@ def test_unaligned_large_sampled_rows():
     (40, 20, 70016),     # 1 tile of 547 stages: pieces cross the 65536-element chunk bound
     (300, 271, 4096),    # output rows not 16-byte aligned: pieces add with atomics
     (1792, 2112, 2048),  # 77 tiles: one wave whole, 1 tile split, zeroed band shared
+    (300, 400, 4032),    # a ragged last stage (K % 128 = 64) inside the last pieces
 ])
 def test_split_schedule_forward(M, N, K):
     A, w, _ = inputs(M, N, K, seed=M + 3 * N + K)
@@ -374,6 +375,7 @@ def test_split_schedule_forward(M, N, K):
     (40, 70016, 64),     # 547 stages, the chunk bound inside pieces
     (300, 4096, 447),    # dX rows not 16-byte aligned: atomic adds
     (1792, 2048, 2112),  # 77 tiles: one wave whole, the rest split
+    (300, 4032, 448),    # a ragged last stage of the reduction (N % 128 = 64)
 ])
 def test_split_schedule_dx(M, N, K):
     _, w, dY = inputs(M, N, K, seed=7 * M + N + K)
