@@ -43,9 +43,9 @@ namespace dw2 {
 constexpr int BMP = 256;        // dW rows (k) per pair tile, 128 per CTA
 constexpr int BN = 256;         // dW columns (n) per pair tile, 128 per CTA
 constexpr int BNH = BN / 2;
-constexpr int BK = 64;          // reduction elements (m) per stage
-constexpr int RAW_STAGES = 4;
-constexpr int OP_STAGES = 4;    // converted stages: the converter-to-MMA hand-off is latency-bound
+constexpr int BK = 128;         // reduction elements (m) per stage
+constexpr int RAW_STAGES = 2;
+constexpr int OP_STAGES = 2;    // converted stages (64 KB each)
 constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512
 constexpr int kConvWarps = 16;            // 8 for A, 8 for dY
@@ -57,11 +57,11 @@ constexpr int kThreads = 32 * (kConvWarps + 2 + 4);
 constexpr int kEpiBarrier = 1;
 constexpr int kChunkElems = 1024;  // exact f32 chunk for int8 x int8 (|sum| <= 2^24)
 
-constexpr int RAW_OP = BK * 128;            // one operand's raw box [64 m][128 B]
+constexpr int RAW_OP = BK * 128;            // one operand's raw box [128 m][128 B]
 constexpr int RAW_STAGE = 2 * RAW_OP;       // A then dY
 constexpr int MN_ATOM = 1024;               // 8 m rows x 128 B
 constexpr int K_GROUP = 2 * MN_ATOM;        // two MN atoms (128 f16) per 8 m rows
-constexpr int OP_OPERAND = (BK / 8) * K_GROUP;  // 16 KB of f16 per operand
+constexpr int OP_OPERAND = (BK / 8) * K_GROUP;  // 32 KB of f16 per operand
 constexpr int OP_STAGE = 2 * OP_OPERAND;
 constexpr int STAGE_OUT = 128 * 32 * 4;
 constexpr int OFF_OP = 0;
@@ -148,7 +148,7 @@ __host__ __device__ constexpr uint32_t idesc_f16_mn(int m, int n) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-// One unit of one operand's stage: raw int8 row m (of 64), 16-byte chunk c
+// One unit of one operand's stage: raw int8 row m (of 128), 16-byte chunk c
 // (16 MN values) -> two 8-value f16 chunks 2c, 2c+1 of MN-major atom c/4.
 // Threads c >= 4 write their odd chunk first so that each 8-thread store
 // phase hits 8 distinct bank groups.
@@ -170,8 +170,8 @@ __device__ __forceinline__ void widen_unit(uint4 x, int m, int c, uint8_t* op) {
   sts128(row + ((g ^ r) << 4), second);
 }
 
-// One operand of one stage: raw int8 [64 m][128 MN] -> f16 MN-major atoms.
-// Unit u = (row m, 16-byte raw chunk c), two per thread.
+// One operand of one stage: raw int8 [128 m][128 MN] -> f16 MN-major atoms.
+// Unit u = (row m, 16-byte raw chunk c), four per thread.
 __device__ __forceinline__ void widen_mn(const uint8_t* raw, uint8_t* op, int tid) {
   constexpr int kUnits = BK * 8;
 #pragma unroll
@@ -181,7 +181,7 @@ __device__ __forceinline__ void widen_mn(const uint8_t* raw, uint8_t* op, int ti
   }
 }
 constexpr int kUnitsPerThread = BK * 8 / kHalfThreads;
-static_assert(kUnitsPerThread == 2, "two units per converter thread");
+static_assert(kUnitsPerThread == 4, "four units per converter thread");
 
 // kGlobal: the instantiation whose converters load the operands from global
 // memory (no raw stages, an idle producer).
@@ -256,7 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int64_t k1 = min(p.num_stages, (c + 1) * kChunkStages);
       for (int64_t kb = c * kChunkStages; kb < k1; ++kb) {
         if (kGlobal) {
-          // this stage's two units go in flight before the wait for the slot
+          // this stage's units go in flight before the wait for the slot
           const int tr = tile / p.tiles_c, tcol = tile % p.tiles_c;
           uint4 x[kUnitsPerThread];
 #pragma unroll
