@@ -427,6 +427,42 @@ __host__ __device__ constexpr int dx_column(int e) {
   return (e & 16) | ((e & 1) << 3) | ((e & 15) >> 1);
 }
 
+// Its inverse: the output column held by accumulator column j.
+__host__ __device__ constexpr int dx_slot(int j) {
+  return (j & 16) | ((j & 7) << 1) | ((j >> 3) & 1);
+}
+
+__host__ __device__ constexpr bool dx_slot_inverts_dx_column() {
+  for (int e = 0; e < 32; ++e)
+    if (dx_slot(dx_column(e)) != e) return false;
+  return true;
+}
+static_assert(dx_slot_inverts_dx_column(), "dx_slot must invert dx_column");
+
+// 32 accumulator columns of a block into v[0..31] in output-column order:
+// for dX each loaded column is bound straight to the register of the output
+// column it holds (v[e] = accumulator column dx_column(e)), so undoing the
+// weight decode's order costs no moves and no second array.
+template <int OP>
+__device__ __forceinline__ void tmem_ld_block(uint32_t taddr, uint32_t (&v)[32]) {
+  if (OP == kOpFwd) {
+    tmem_ld_32x32b_x32(taddr, v);
+    return;
+  }
+#define T3_SLOT(j) "=r"(v[dx_slot(j)])
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : T3_SLOT(0), T3_SLOT(1), T3_SLOT(2), T3_SLOT(3), T3_SLOT(4), T3_SLOT(5), T3_SLOT(6),
+        T3_SLOT(7), T3_SLOT(8), T3_SLOT(9), T3_SLOT(10), T3_SLOT(11), T3_SLOT(12), T3_SLOT(13),
+        T3_SLOT(14), T3_SLOT(15), T3_SLOT(16), T3_SLOT(17), T3_SLOT(18), T3_SLOT(19), T3_SLOT(20),
+        T3_SLOT(21), T3_SLOT(22), T3_SLOT(23), T3_SLOT(24), T3_SLOT(25), T3_SLOT(26), T3_SLOT(27),
+        T3_SLOT(28), T3_SLOT(29), T3_SLOT(30), T3_SLOT(31)
+      : "r"(taddr));
+#undef T3_SLOT
+}
+
 __device__ __forceinline__ void w_dx_load(const uint8_t* raw_w, int tid, uint32_t rank,
                                           uint32_t (&v)[32]) {
 #pragma unroll
@@ -914,17 +950,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int64_t col0 = static_cast<int64_t>(tcol) * BN + cb * 32;
           if (col0 >= p.out_cols) break;
           uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + ab * BN +
-                                 cb * 32,
-                             v);
+          tmem_ld_block<OP>(
+              tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + ab * BN + cb * 32, v);
           tmem_wait_ld();
-          if (OP == kOpDx) {  // undo the weight decode's column order
-            uint32_t t[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) t[e] = v[dx_column(e)];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = t[e];
-          }
           if (p.use_tma_out) {
             uint8_t* buf = stage_out + (slab & 1) * L::stage_out;
             if (epi_tid == 0) bulk_wait_group_read<1>();
