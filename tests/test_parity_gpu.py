@@ -404,3 +404,34 @@ def test_split_schedule_chained_calls_see_earlier_outputs():
     assert_same(c0, oracle.fwd(A0, wp0), "split chained call 1")
     assert_same(c1, oracle.fwd(c0.view(np.int8).reshape(300, 1600), wp1), "split chained call 2")
     assert_same(c2, oracle.fwd(A2, c1.view(np.uint8).reshape(300, 1088)), "split chained call 3")
+
+
+def test_random_long_reduction_shapes():
+    """Random few-tile shapes with long reductions (most take the split
+    schedule, with pieces of random lengths and boundaries), fwd and dX, in
+    full against the oracle."""
+    g = np.random.default_rng(2026)
+    for it in range(8):
+        M = int(g.integers(33, 700))
+        N = int(g.integers(1, 6)) * 64 + int(g.integers(0, 2)) * 32
+        K = int(g.integers(8, 80)) * 64
+        A, w, dY = inputs(M, N, K, seed=9000 + it)
+        wp = oracle.pack(w)
+        assert_same(run_fwd(A, wp), oracle.fwd(A, wp), f"fwd {M}x{N}x{K}")
+        _, w2, dY2 = inputs(M, K, N, seed=9100 + it)   # dX over a K-long reduction
+        wp2 = oracle.pack(w2)
+        assert_same(run_dx(dY2, wp2, N), oracle.dx(dY2, wp2, N), f"dX {M}x{K}x{N}")
+
+
+def test_random_dw_shapes():
+    """dW over random reductions (partial 128-row stages, 1024-row chunk
+    boundaries, a second chunk of any length) and random widths (TMA-aligned
+    or not), in full against the oracle."""
+    g = np.random.default_rng(77)
+    for it in range(8):
+        M = int(g.integers(1, 3000))
+        K = int(g.integers(1, 400)) if it % 2 else int(g.integers(1, 25)) * 16
+        N = int(g.integers(1, 400)) if it % 3 == 2 else int(g.integers(1, 25)) * 16
+        A = t3_synth.int8_uniform(t3_synth.rng(9200 + it), (M, K))
+        dY = t3_synth.int8_uniform(t3_synth.rng(9300 + it), (M, N))
+        assert_same(run_dw(A, dY), oracle.dw(A, dY), f"dW {M}x{N}x{K}")
