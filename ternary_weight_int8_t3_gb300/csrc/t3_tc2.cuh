@@ -281,18 +281,6 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// 16 codes (code i at bits 2i) -> 8 f16x2 words in the permuted reduction
-// order: word 2j = (code j, code j+4), word 2j+1 = (code j+8, code j+12).
-__device__ __forceinline__ void decode16_pairs(uint32_t x, uint32_t* o) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t sh = (j < 3) ? (x << (4 - 2 * j)) : (x >> 2);
-    const uint32_t s = (sh & 0x30303030u) | 0x04040404u;
-    o[2 * j] = prmt(tc::kF16HiTable, 0u, s);
-    o[2 * j + 1] = prmt(tc::kF16HiTable, 0u, s >> 16);
-  }
-}
-
 // ------------------------------------------------------------ converters
 
 // Four int8 b0..b3 -> f16x2 words (b0, b2) and (b1, b3), exact (same bias
