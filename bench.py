@@ -71,6 +71,23 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+def max_over_ranks(x, pg, device):
+    """The largest of every rank's x (a time): the whole job takes as long as
+    its slowest rank.  pg is torch.distributed (initialised) or None."""
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tops(ms_per_step, world):
+    """Whole-job throughput: every rank runs one layer step (three products)
+    per step, so the units all ranks processed over the slowest rank's time."""
+    return 3 * OPS_PER_PRODUCT * world / (ms_per_step * 1e-3) / 1e12
+
+
 def make_host_inputs():
     g = t3_synth.rng(SEED)
     A = t3_synth.int8_uniform(g, (M, K))
@@ -494,11 +511,7 @@ def main():
     if rc != t3.T3_OK:
         raise RuntimeError(f"device wait timed out during the bench ({detail:#x})")
 
-    elapsed_max = elapsed_ms
-    if pg is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_max = float(t.item())
+    elapsed_max = max_over_ranks(elapsed_ms, pg, dev)
 
     # ---- end to end: pinned host inputs in, results out, every step
     A_h = torch.from_numpy(A).pin_memory()
@@ -574,11 +587,7 @@ def main():
     t2.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = s2.elapsed_time(t2) / e2e_steps
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(s2.elapsed_time(t2) / e2e_steps, pg, dev)
     h2d = A.nbytes + wp.nbytes + dY.nbytes
     d2h = (M * N + M * K + K * N) * 4
 
@@ -588,7 +597,7 @@ def main():
         return
 
     ms_step = elapsed_max / args.steps
-    value = 3 * OPS_PER_PRODUCT * world / (ms_step * 1e-3) / 1e12
+    value = job_tops(ms_step, world)
     avg = {k: sum(v) / len(v) for k, v in per.items()}
     op_tops = {k: OPS_PER_PRODUCT / (avg[k] * 1e-3) / 1e12 for k in avg}
     dominant = max(avg, key=avg.get)
@@ -616,7 +625,7 @@ def main():
                      "peak": peak, "unit": "TFLOP/s", "frac": op_tops[dominant] / peak,
                      "traffic": traffic, "peak_source": peak_note},
         "gpu_launches": 4 * args.steps,  # fwd, dX, dW zeroing + dW product
-        "e2e": {"value": 3 * OPS_PER_PRODUCT * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": job_tops(e2e_ms, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host buffers; every step copies its inputs in and C, dX, dW out "
                        "on streams of their own, overlapping the kernels and each other (two "
