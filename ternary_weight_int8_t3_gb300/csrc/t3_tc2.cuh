@@ -113,9 +113,10 @@ struct Params {
   int mode;               // kernel instantiation: kModeTma, kModeWGlobal, kModeAGlobal
   // Schedule: tiles [0, dp_tiles) are taken whole, round-robin over the
   // pairs; the (tile, stage) iterations of the remaining tiles are split into
-  // equal contiguous ranges, one per pair (stream-K).  Those pieces add their
-  // int32 sums onto output rows that a chained grid has zeroed; when
-  // dp_tiles < tiles_r * tiles_c every output write waits for that grid.
+  // equal contiguous ranges, one per pair (stream-K), which each pair works
+  // through before its whole tiles.  Those pieces add their int32 sums onto
+  // output rows that a chained grid has zeroed; when dp_tiles < tiles_r *
+  // tiles_c every output write waits for that grid.
   int dp_tiles;
   int* err;
 };
@@ -127,29 +128,36 @@ struct Piece {
   int tile, kb0, kb1;
 };
 
-// Piece i (0, 1, ...) of a pair: first the whole tiles pair, pair + npairs, ...
-// below dp_tiles, then the pair's equal share of the remaining tiles'
-// (tile, stage) iterations, cut at tile boundaries.  False past the last one.
-// 32-bit indices suffice: a reduction has at most 131072 stages and the split
-// part fewer than npairs tiles.
+// Piece i (0, 1, ...) of a pair: first the pair's equal share of the split
+// tiles' (tile, stage) iterations, cut at tile boundaries (at most two
+// pieces: a share is shorter than a tile), then the whole tiles pair,
+// pair + npairs, ... below dp_tiles.  With the split pieces first, their
+// adding flushes overlap the whole tiles' work and a pair's last flush is a
+// plain store.  False past the last piece.  32-bit indices suffice: a
+// reduction has at most 131072 stages and the split part fewer than npairs
+// tiles.
 __device__ __forceinline__ bool get_piece(const Params& p, int pair, int npairs, int i, Piece& w) {
   const int S = static_cast<int>(p.num_stages);
-  const int whole = pair < p.dp_tiles ? (p.dp_tiles - 1 - pair) / npairs + 1 : 0;
-  if (i < whole) {
-    w.tile = pair + i * npairs;
-    w.kb0 = 0;
-    w.kb1 = S;
-    return true;
-  }
+  // first the pair's share [b, e) of the split tiles' iterations, cut at tile
+  // boundaries (their flushes add, and overlap the whole tiles after them)
   const int64_t total = static_cast<int64_t>(p.tiles_r * p.tiles_c - p.dp_tiles) * S;
   const int b = static_cast<int>(total * pair / npairs);
   const int e = static_cast<int>(total * (pair + 1) / npairs);
-  const int t = b / S + (i - whole);  // split tile, counted from dp_tiles
-  const int s0 = t * S > b ? t * S : b;
-  if (s0 >= e) return false;
-  w.tile = p.dp_tiles + t;
-  w.kb0 = s0 - t * S;
-  w.kb1 = (e - t * S < S) ? e - t * S : S;
+  const int n_sk = b < e ? (e - 1) / S - b / S + 1 : 0;
+  if (i < n_sk) {
+    const int t = b / S + i;  // split tile, counted from dp_tiles
+    const int s0 = t * S > b ? t * S : b;
+    w.tile = p.dp_tiles + t;
+    w.kb0 = s0 - t * S;
+    w.kb1 = (e - t * S < S) ? e - t * S : S;
+    return true;
+  }
+  // then the whole tiles pair, pair + npairs, ... below dp_tiles
+  const int tile = pair + (i - n_sk) * npairs;
+  if (tile >= p.dp_tiles) return false;
+  w.tile = tile;
+  w.kb0 = 0;
+  w.kb1 = S;
   return true;
 }
 
