@@ -95,6 +95,11 @@ int t3_pack_ternary_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N,
  * that zeroes C and one that adds the product into it; the second may start
  * before the first ends (programmatic dependent launch) but touches C only
  * after it, and the first touches C only after all earlier work on `stream`.
+ * For M > 32, when whole output tiles would leave most of the GPU idle over a
+ * long reduction (few tiles, many reduction stages) and A and Wp are
+ * TMA-addressable, the reduction of the last tiles is split over the whole
+ * GPU: the call then enqueues the same pair of kernels, the first zeroing the
+ * rows of C that the split part adds into.
  */
 int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,
                 int64_t K, t3_stream_t stream);
@@ -103,6 +108,8 @@ int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64
  * t3_gemm_bwd_dx -- [bwd] kernel 1: dX[m][k] = sum_{n<N} dY[m][n] * W[k][n].
  *   dY [M][N], Wp [N][ceil(K/4)] (the forward's packed weights), dX [M][K].
  * Exact for every input when N <= 16777215; larger N returns T3_EOVERFLOW.
+ * Long reductions over few output tiles are split as in t3_gemm_fwd (M > 32),
+ * with a zeroing kernel before the product.
  */
 int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, int64_t N,
                    int64_t K, t3_stream_t stream);
@@ -112,10 +119,9 @@ int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, 
  *   A [M][K], dY [M][N], dW [K][N].
  * int8 x int8 products reach 16384, so the reduction is exact in int32 only
  * for M <= 131071 (the pages' bound); larger M returns T3_EOVERFLOW.
- * When every operand is TMA-addressable (16-byte aligned bases, N and K
- * multiples of 16) it enqueues two kernels on `stream`: one that zeroes dW and
- * one that adds 1024-row partial sums into it, with the same ordering as the
- * small-M forward above; otherwise one kernel that writes dW.
+ * It enqueues two kernels on `stream`: one that zeroes dW and one that adds
+ * 1024-row partial sums into it, with the same ordering as the small-M
+ * forward above.
  */
 int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N,
                    int64_t K, t3_stream_t stream);
@@ -224,8 +230,8 @@ const char* t3_status_string(int status);
  * value.  *detail, when not NULL, receives the recorded code (0 if none):
  * bits 0-7 the role (1 producer, 2 converter, 3 MMA issuer, 4 epilogue,
  * 5 pair forwarder gave up; 6 an input value was invalid), bits 8-15 the
- * kernel (1 fwd, 2 dX, 3 dW on one CTA per tile; 4 small-M fwd; 5 fwd, 6 dX,
- * 7 dW on CTA pairs; 9 the device packer).
+ * kernel (4 small-M fwd; 5 fwd, 6 dX, 7 dW on CTA pairs; 9 the device
+ * packer).
  */
 int t3_last_device_error(t3_stream_t stream, int32_t* detail);
 
