@@ -304,7 +304,16 @@ def test_empty_reduction_writes_zeros():
     C = torch.full((5, 7), 3, dtype=torch.int32, device="cuda")
     t3.t3_gemm_fwd(torch.empty((5, 0), dtype=torch.int8, device="cuda"),
                    torch.empty((7, 0), dtype=torch.uint8, device="cuda"), K=0, C=C)
-    assert torch.count_nonzero(C).item() == 0
+    # dX over an empty N and dW over an empty M: zeros, whatever was there
+    dX = torch.full((5, 9), 3, dtype=torch.int32, device="cuda")
+    t3.t3_gemm_bwd_dx(torch.empty((5, 0), dtype=torch.int8, device="cuda"),
+                      torch.empty((0, 3), dtype=torch.uint8, device="cuda"), 9, dX=dX)
+    dW = torch.full((6, 4), 3, dtype=torch.int32, device="cuda")
+    t3.t3_gemm_bwd_dw(torch.empty((0, 6), dtype=torch.int8, device="cuda"),
+                      torch.empty((0, 4), dtype=torch.int8, device="cuda"), dW=dW)
+    torch.cuda.synchronize()
+    for out in (C, dX, dW):
+        assert torch.count_nonzero(out).item() == 0
 
 
 @pytest.mark.parametrize("M,N,K", [(512, 1024, 4000), (300, 4000, 1008), (257, 336, 272)])
