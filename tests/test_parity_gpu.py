@@ -444,3 +444,24 @@ def test_random_dw_shapes():
         A = t3_synth.int8_uniform(t3_synth.rng(9200 + it), (M, K))
         dY = t3_synth.int8_uniform(t3_synth.rng(9300 + it), (M, N))
         assert_same(run_dw(A, dY), oracle.dw(A, dY), f"dW {M}x{N}x{K}")
+
+
+def test_million_term_reductions():
+    """Reductions of 2^20 terms (16 exact f32 chunks of 65536, spread over
+    every CTA pair by the split schedule): extreme values, whose sum 128 * 2^20
+    is exact only if every chunk is added in int32, and random values against
+    the oracle, for the forward and dX."""
+    R = 1 << 20
+    A = np.full((40, R), -128, dtype=np.int8)
+    wp = t3.t3_pack_ternary(-np.ones((R, 16), dtype=np.int8))
+    assert np.all(run_fwd(A, wp) == 128 * R)
+    dY = np.full((40, R), -128, dtype=np.int8)
+    wp_dx = t3.t3_pack_ternary(-np.ones((64, R), dtype=np.int8))
+    assert np.all(run_dx(dY, wp_dx, 64) == 128 * R)
+    g = t3_synth.rng(1 << 20)
+    A2 = t3_synth.int8_uniform(g, (33, R))
+    wp2 = oracle.pack(t3_synth.ternary(g, (R, 8)))
+    assert_same(run_fwd(A2, wp2), oracle.fwd(A2, wp2), "fwd 33x8x2^20")
+    dY2 = t3_synth.int8_uniform(g, (33, R))
+    wp3 = oracle.pack(t3_synth.ternary(g, (64, R)))
+    assert_same(run_dx(dY2, wp3, 64), oracle.dx(dY2, wp3, 64), "dX 33x2^20x64")
