@@ -465,3 +465,17 @@ def test_million_term_reductions():
     dY2 = t3_synth.int8_uniform(g, (33, R))
     wp3 = oracle.pack(t3_synth.ternary(g, (64, R)))
     assert_same(run_dx(dY2, wp3, 64), oracle.dx(dY2, wp3, 64), "dX 33x2^20x64")
+
+
+def test_dw_at_the_row_bound():
+    """dW over the pages' largest reduction, 131071 rows (128 exact chunks of
+    1024): -128 * -128 on every row sums to 2147467264, just inside int32;
+    random values there against the oracle."""
+    Mb = 131071
+    A = np.full((Mb, 16), -128, dtype=np.int8)
+    dY = np.full((Mb, 32), -128, dtype=np.int8)
+    assert np.all(run_dw(A, dY) == 16384 * Mb)
+    g = t3_synth.rng(Mb)
+    A2 = t3_synth.int8_uniform(g, (Mb, 16))
+    dY2 = t3_synth.int8_uniform(g, (Mb, 48))
+    assert_same(run_dw(A2, dY2), oracle.dw(A2, dY2), "dW 131071 rows")
