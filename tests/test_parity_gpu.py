@@ -371,6 +371,8 @@ def test_unaligned_large_sampled_rows():
     (300, 271, 4096),    # output rows not 16-byte aligned: pieces add with atomics
     (1792, 2112, 2048),  # 77 tiles: one wave whole, 1 tile split, zeroed band shared
     (300, 400, 4032),    # a ragged last stage (K % 128 = 64) inside the last pieces
+    (1792, 2111, 2048),  # 77 tiles, output rows not 16-byte aligned: plain stores of the
+                         # whole tiles in the zeroed band, atomic adds for the split one
 ])
 def test_split_schedule_forward(M, N, K):
     A, w, _ = inputs(M, N, K, seed=M + 3 * N + K)
