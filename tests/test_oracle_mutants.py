@@ -179,3 +179,43 @@ def test_quantizer_pins_catch_planted_mistake(name, monkeypatch):
         except AssertionError:
             caught += 1
     assert caught > 0, f"no quantizer pin caught mutant {name}"
+
+
+def _m_divides_by_scales(x, row_scale=None, col_scale=None, kind=0, out=None):
+    import numpy as np
+    x = np.asarray(x, np.int32)
+    rows, cols = x.shape
+    rs = np.ones(rows, np.float32) if row_scale is None else np.asarray(row_scale, np.float32)
+    cs = np.ones(cols, np.float32) if col_scale is None else np.asarray(col_scale, np.float32)
+    return _finish((x.astype(np.float32) / rs[:, None]) / cs[None, :], kind, out)
+
+
+def _m_scale_is_amax(x_bits):
+    import numpy as np
+    q, s = _ORIG_QUANT(x_bits)
+    return q, (s * np.float32(127.0)).astype(np.float32)
+
+
+_ORIG_QUANT = _oracle_mod.quantize_rows
+
+CHAIN_MUTANTS = {
+    "dequant_divides_by_scales": ("dequant", _m_divides_by_scales),
+    "quant_reports_amax_as_scale": ("quantize_rows", _m_scale_is_amax),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CHAIN_MUTANTS))
+def test_chain_pins_catch_planted_mistake(name, monkeypatch):
+    """The f64-bound pins of quantize -> product -> dequantize catch mistakes
+    in what the chain means, on their own."""
+    import test_oracle_pins as pins
+    attr, fn = CHAIN_MUTANTS[name]
+    monkeypatch.setattr(_oracle_mod, attr, fn)
+    caught = 0
+    for pin in (pins.test_quantized_forward_within_f64_bound, pins.test_quantized_dx_within_f64_bound,
+                pins.test_quantized_dw_within_f64_bound):
+        try:
+            pin()
+        except AssertionError:
+            caught += 1
+    assert caught == 3, f"the chain pins caught mutant {name} {caught} times of 3"

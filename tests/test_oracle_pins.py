@@ -416,3 +416,75 @@ def test_quantize_rows_properties():
     assert np.all(np.abs(q[np.arange(64), am]) == 127)       # the row's maximum maps to +-127
     err = np.abs(q * s[:, None].astype(np.float64) - xf)
     assert np.all(err <= s[:, None] * 0.5 * (1 + 1e-5))       # half a step, plus float slack
+
+
+# ------------------------------------------- the quantized chain against f64 --
+# Quantize, take the exact integer product, dequantize: the result must stay
+# within the quantization error of the f64 product of the original values
+# (the pages bounded their quantized backward against an f64 reference).  Each
+# element of a row quantized with scale s is off by at most s / 2 (plus a few
+# float32 ulps of |x|); the dequantization adds a few ulps of the result.
+
+def _bf16_matrix(g, shape, spread=True):
+    mag = np.float32(2.0) ** g.integers(-6, 7, (shape[0], 1)).astype(np.float32) if spread else 1.0
+    x = (g.standard_normal(shape) * mag).astype(np.float32)
+    bits = oracle.bf16_bits(x)
+    return bits, (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _ulps(v):
+    return 4.0 * np.finfo(np.float32).eps * v
+
+
+def test_quantized_forward_within_f64_bound():
+    g = t3_synth.rng(4101)
+    M, K, N = 48, 320, 40
+    bits, x = _bf16_matrix(g, (M, K))
+    w = t3_synth.ternary(g, (K, N))
+    q, s = oracle.quantize_rows(bits)
+    y = oracle.dequant(oracle.fwd(q, oracle.pack(w)), s, None).astype(np.float64)
+    wf = w.astype(np.float64)
+    truth = x @ wf
+    bound = (s.astype(np.float64)[:, None] / 2) * (np.abs(wf).sum(0)[None, :]) \
+        + _ulps(np.abs(x) @ np.abs(wf)) + _ulps(np.abs(truth))
+    err = np.abs(y - truth)
+    assert np.all(err <= bound)
+    assert err.max() > 0  # the bound is not met trivially
+
+
+def test_quantized_dx_within_f64_bound():
+    g = t3_synth.rng(4102)
+    M, N, K = 40, 288, 56
+    bits, dy = _bf16_matrix(g, (M, N))
+    w = t3_synth.ternary(g, (K, N))
+    q, s = oracle.quantize_rows(bits)
+    y = oracle.dequant(oracle.dx(q, oracle.pack(w), K), s, None).astype(np.float64)
+    wf = w.astype(np.float64)
+    truth = dy @ wf.T
+    bound = (s.astype(np.float64)[:, None] / 2) * (np.abs(wf).sum(1)[None, :]) \
+        + _ulps(np.abs(dy) @ np.abs(wf.T)) + _ulps(np.abs(truth))
+    err = np.abs(y - truth)
+    assert np.all(err <= bound)
+    assert err.max() > 0
+
+
+def test_quantized_dw_within_f64_bound():
+    """dW with X and dY quantized per column (the scales the pages name for
+    dW): dequant(dW(qX, qdY), sX as row scale, sdY as column scale)."""
+    g = t3_synth.rng(4103)
+    M, K, N = 200, 24, 32
+    xb, x = _bf16_matrix(g, (M, K), spread=False)
+    yb, dy = _bf16_matrix(g, (M, N), spread=False)
+    qxt, sx = oracle.quantize_rows(np.ascontiguousarray(xb.T))
+    qyt, sy = oracle.quantize_rows(np.ascontiguousarray(yb.T))
+    qx, qy = np.ascontiguousarray(qxt.T), np.ascontiguousarray(qyt.T)
+    y = oracle.dequant(oracle.dw(qx, qy), sx, sy).astype(np.float64)
+    truth = x.T @ dy
+    sxd, syd = sx.astype(np.float64), sy.astype(np.float64)
+    # a dy - qa sa qd sd = a ed + ea qd sd, |ea| <= sa/2, |ed| <= sd/2, |qd sd| <= |dy| + sd/2
+    bound = np.abs(x).T @ np.ones((M, N)) * (syd[None, :] / 2) \
+        + (sxd[:, None] / 2) * (np.ones((K, M)) @ (np.abs(dy) + syd[None, :] / 2)) \
+        + _ulps(np.abs(x).T @ np.abs(dy)) + _ulps(np.abs(truth))
+    err = np.abs(y - truth)
+    assert np.all(err <= bound)
+    assert err.max() > 0
