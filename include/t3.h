@@ -36,9 +36,15 @@
  *     returns T3_OK.  A call whose reduction is empty (K = 0 for the forward,
  *     N = 0 for dX, M = 0 for dW) writes zeros to its output.
  *   - Argument errors are reported before anything is launched; nothing is
- *     written then.  No C++ exception crosses this interface and the device
- *     code never traps.
+ *     written then.  After T3_ECUDA (a launch or attribute call failed) the
+ *     contents of the output are undefined: a call that queues a zeroing
+ *     kernel before its product may have queued it already.  No C++
+ *     exception crosses this interface and the device code never traps.
  *   - Calls may be made from several host threads; each call is independent.
+ *   - Per-device state (the device error word's address, kernel attributes,
+ *     the no-alloc buffer's address) is resolved once per device and process.
+ *     It does not survive cudaDeviceReset: do not call the library on a device
+ *     again in a process that reset it.
  */
 #ifndef T3_H_
 #define T3_H_
@@ -209,7 +215,14 @@ int t3_gemm_bwd_dw_scaled(const int8_t* A, const int8_t* dY, void* dW, int64_t M
  *   host threads without ordering; each call's stream order alone protects
  *   only calls on that stream.
  *   The first call on each device resolves the buffer's address
- *   (cudaGetSymbolAddress); make that call outside any stream capture.
+ *   (cudaGetSymbolAddress); make that call outside any stream capture.  The
+ *   address, like all per-device state, is not valid after cudaDeviceReset.
+ *   Residency: the buffer sits in a module of its own.  With CUDA's lazy
+ *   module loading (the default) a device reserves its 32 MiB at the first
+ *   call of this function there and keeps it until the process exits; the
+ *   other entry points do not load that module.  With eager loading
+ *   (CUDA_MODULE_LOADING=EAGER) every device reserves it when the library's
+ *   modules load.
  * Arguments, sizes, results and other errors are those of
  * t3_gemm_bwd_dw_scaled.
  */
@@ -231,9 +244,22 @@ const char* t3_status_string(int status);
  * bits 0-7 the role (1 producer, 2 converter, 3 MMA issuer, 4 epilogue,
  * 5 pair forwarder gave up; 6 an input value was invalid), bits 8-15 the
  * kernel (4 small-M fwd; 5 fwd, 6 dX, 7 dW on CTA pairs; 9 the device
- * packer).
+ * packer; 10 the wait self-test below).
  */
 int t3_last_device_error(t3_stream_t stream, int32_t* detail);
+
+/*
+ * t3_selftest_wait_timeout -- exercises the bounded-wait path above without
+ * any fault: one CTA waits on a pipeline barrier that nothing completes, with
+ * the kernels' own wait loop but a limit of `limit_ns` nanoseconds of device
+ * time instead of two seconds.  The wait gives up, records (10 << 8) | 2 in
+ * the error word (unless a code is already there) and the kernel returns, so
+ * the next t3_last_device_error reports T3_ETIMEOUT with that detail and the
+ * device stays usable.  The pages have no counterpart: this is a check of the
+ * library's failure reporting.  limit_ns must lie in [1000, 2e9], else
+ * T3_EINVAL; asynchronous on `stream`.
+ */
+int t3_selftest_wait_timeout(int64_t limit_ns, t3_stream_t stream);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int t3_version(void);

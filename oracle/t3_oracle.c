@@ -18,7 +18,7 @@
  *           layout) and kernel 2 (dW = X^T x dY summed over rows, int32
  *           accumulation, reduction length <= 131071).
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *   - code layout: the code of W[k][n] sits in byte (n * ceil(K/4) + k/4) of Wp,
  *     at bits 2*(k%4); the rows of Wp are n, each ceil(K/4) bytes, no padding.
  *   - the packer takes w as int8 [K][N] row-major and writes code 0 into the pad

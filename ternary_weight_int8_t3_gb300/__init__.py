@@ -81,6 +81,8 @@ def load():
         lib.t3_status_string.restype = ctypes.c_char_p
         lib.t3_last_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
         lib.t3_last_device_error.restype = ctypes.c_int
+        lib.t3_selftest_wait_timeout.argtypes = [i64, p]
+        lib.t3_selftest_wait_timeout.restype = ctypes.c_int
         lib.t3_version.argtypes = []
         lib.t3_version.restype = ctypes.c_int
         _lib = lib
@@ -375,6 +377,16 @@ def t3_last_device_error(stream=None):
     detail = ctypes.c_int32(0)
     rc = load().t3_last_device_error(ctypes.c_void_p(s.cuda_stream), ctypes.byref(detail))
     return rc, detail.value
+
+
+def t3_selftest_wait_timeout(limit_ns: int, stream=None):
+    """Launches the bounded-wait self-test: one CTA waits on a barrier that
+    nothing completes and gives up after limit_ns of device time, recording
+    its code for t3_last_device_error."""
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(load().t3_selftest_wait_timeout(int(limit_ns), ctypes.c_void_p(s.cuda_stream)),
+           "t3_selftest_wait_timeout")
 
 
 def t3_version() -> int:

@@ -141,6 +141,22 @@ int device_info(const DeviceInfo** out) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// One CTA waits on a barrier that nothing completes, with the pipelines' wait
+// (suspend hints, abort flag, error word) but a limit of limit_ns: it must
+// give up, record (10 << 8) | 2 in the error word and return.
+__global__ void wait_selftest_kernel(int* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    mbar_wait_limit(&bar, 0, &abort_flag, err, (10 << 8) | 2, limit_ns);
+}
+
 // The CTA-pair pipeline for the forward (OP = kOpFwd: act = A [M][K], weights
 // packed along K) or dX (act = dY [M][N], reduction N), for operands of any
 // alignment.  A scaled output kind needs bulk stores and the reduction in one
@@ -220,6 +236,10 @@ int run_tc2(const int8_t* act, const uint8_t* Wp, void* out, int64_t M, int64_t 
   p.dp_tiles = static_cast<int>(dp_tiles);
   const bool split = dp_tiles < num_tiles;
   if (split) {
+    // the split kernel's attributes first, so that a failure there leaves the
+    // output untouched
+    st = (OP == kOpFwd) ? prepare_tc2_fwd() : prepare_tc2_dx();
+    if (st != T3_OK) return st;
     // from the first tile row that holds a split tile to the end
     const int64_t row0 = (dp_tiles / tiles_c) * tc2::BMP;
     st = launch_zero_pdl(static_cast<int32_t*>(out) + row0 * out_cols, (M - row0) * out_cols,
@@ -458,42 +478,7 @@ int t3_gemm_bwd_dw_scaled(const int8_t* A, const int8_t* dY, void* dW, int64_t M
 
 }  // extern "C"
 
-namespace t3 {
-namespace {
-
-// The int32 intermediate of t3_gemm_bwd_dw_scaled_noalloc: a fixed device
-// buffer of 8 Mi entries (32 MiB) per device, enough for dW up to K * N =
-// 8,388,608 (the 1280 x 3456 layer's dW has 4,423,680).  Nothing in it has to
-// start at zero: the dW product writes every entry of its K x N block before
-// the dequantization reads it.  Every call on a device shares it.
-constexpr int64_t kNoAllocWorkspaceEntries = 8LL * 1024 * 1024;
-std::atomic<int32_t*> g_noalloc_addr[kMaxDevices];  // resolved once per device
-
-}  // namespace
-
-static __device__ __align__(256) int32_t g_noalloc_workspace[kNoAllocWorkspaceEntries];
-
-}  // namespace t3
-
 extern "C" {
-
-int t3_gemm_bwd_dw_scaled_noalloc(const int8_t* A, const int8_t* dY, void* dW, int64_t M,
-                                  int64_t N, int64_t K, const float* row_scale,
-                                  const float* col_scale, int out_kind, t3_stream_t stream) {
-  if (bad_dims(M, N, K) || !valid_out_kind(out_kind)) return T3_EINVAL;
-  if (K == 0 || N == 0) return T3_OK;
-  if (K * N > kNoAllocWorkspaceEntries) return T3_EINVAL;  // checked before any CUDA call
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
-  if (dev < 0 || dev >= kMaxDevices) return T3_EDEVICE;
-  int32_t* ws = g_noalloc_addr[dev].load(std::memory_order_acquire);
-  if (!ws) {
-    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ws), g_noalloc_workspace) != cudaSuccess)
-      return T3_ECUDA;
-    g_noalloc_addr[dev].store(ws, std::memory_order_release);
-  }
-  return t3_gemm_bwd_dw_scaled(A, dY, dW, M, N, K, row_scale, col_scale, out_kind, ws, stream);
-}
 
 const char* t3_status_string(int status) {
   switch (status) {
@@ -527,6 +512,15 @@ int t3_last_device_error(t3_stream_t stream, int32_t* detail) {
   return (value & 0xFF) == 6 ? T3_EVALUE : T3_ETIMEOUT;  // role 6: an invalid input value
 }
 
-int t3_version(void) { return 100; }
+int t3_selftest_wait_timeout(int64_t limit_ns, t3_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > static_cast<int64_t>(kWaitLimitNs)) return T3_EINVAL;
+  const DeviceInfo* dev = nullptr;
+  const int st = device_info(&dev);
+  if (st != T3_OK) return st;
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(dev->err_word, static_cast<uint64_t>(limit_ns));
+  return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
+}
+
+int t3_version(void) { return 200; }
 
 }  // extern "C"

@@ -24,6 +24,10 @@ int launch_tc2_fwd(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMa
                    const CUtensorMap& mo, int grid, cudaStream_t s);
 int launch_tc2_dx(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap& mw,
                   const CUtensorMap& mo, int grid, cudaStream_t s);
+// The same kernels' launch attributes, set once per device (launch_tc2_* call
+// these too); the split schedule calls them before it queues its zeroing grid.
+int prepare_tc2_fwd();
+int prepare_tc2_dx();
 
 // Zeroes out[0, n) on `s` as a programmatic dependent of the work before it:
 // it waits for that work to complete, then lets the next grid launch early.

@@ -88,21 +88,29 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
   return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag, int* err, int code) {
+// mbar_wait with the limit as a parameter (the pipelines use kWaitLimitNs;
+// the wait self-test a few milliseconds).
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity,
+                                                volatile int* abort_flag, int* err, int code,
+                                                uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = global_timer_ns();
   for (uint32_t spin = 1;; ++spin) {
     if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;
     if ((spin & 15u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         atomicCAS(err, 0, code);
         *abort_flag = 1;
         return false;
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort_flag, int* err, int code) {
+  return mbar_wait_limit(bar, parity, abort_flag, err, code, kWaitLimitNs);
 }
 
 // ----------------------------------------------------------------------- TMA

@@ -12,9 +12,9 @@
 
 namespace t3 {
 
+// Sets the kernels' shared-memory attributes, once per device.
 template <int OP>
-int launch_tc2_op(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap& mw,
-                  const CUtensorMap& mo, int grid, cudaStream_t s) {
+int prepare_tc2_op() {
   constexpr int kSmem = tc2::Layout<OP>::smem_alloc;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
@@ -32,6 +32,15 @@ int launch_tc2_op(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap
       return T3_ECUDA;
     attr_done[dev].store(true, std::memory_order_release);
   }
+  return T3_OK;
+}
+
+template <int OP>
+int launch_tc2_op(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap& mw,
+                  const CUtensorMap& mo, int grid, cudaStream_t s) {
+  constexpr int kSmem = tc2::Layout<OP>::smem_alloc;
+  const int st = prepare_tc2_op<OP>();
+  if (st != T3_OK) return st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -9,4 +9,6 @@ int launch_tc2_dx(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap
   return launch_tc2_op<kOpDx>(p, ma, mw, mo, grid, s);
 }
 
+int prepare_tc2_dx() { return prepare_tc2_op<kOpDx>(); }
+
 }  // namespace t3

@@ -9,4 +9,6 @@ int launch_tc2_fwd(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMa
   return launch_tc2_op<kOpFwd>(p, ma, mw, mo, grid, s);
 }
 
+int prepare_tc2_fwd() { return prepare_tc2_op<kOpFwd>(); }
+
 }  // namespace t3

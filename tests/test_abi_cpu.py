@@ -40,6 +40,12 @@ def test_library_has_no_oracle_or_cpu_fallback():
                 assert "t3_oracle" not in text and "oracle_" not in text, f
 
 
+def test_selftest_rejects_limits_out_of_range_before_any_cuda_call(lib):
+    f = lib.t3_selftest_wait_timeout
+    for limit in (-1, 0, 999, 2_000_000_001, 1 << 40):
+        assert f(limit, None) == t3.T3_EINVAL
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, -6):
         s = t3.status_string(code)

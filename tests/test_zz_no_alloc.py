@@ -3,6 +3,11 @@ intermediate in the library's fixed per-device buffer instead of a caller
 workspace.  GPU parity against the oracle (every output kind, repeated calls
 that reuse the buffer, the layer's dW size) and the size limit, which is
 checked before any CUDA call.  Collected last (file name)."""
+import json
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 
@@ -77,3 +82,44 @@ def test_noalloc_dw_layer_size_sampled_rows():
     np.testing.assert_array_equal(_bits(res, 1)[rows], _want(x, rs[rows], cs, 1, None))
     rc, detail = t3.t3_last_device_error()
     assert rc == t3.T3_OK, f"device error word set, detail={detail:#x}"
+
+
+_RESIDENCY_PROBE = r"""
+import json, sys
+sys.path.insert(0, sys.argv[1])
+import torch
+import ternary_weight_int8_t3_gb300 as t3
+t3.load()
+dev = torch.device("cuda")
+A = torch.zeros((64, 128), dtype=torch.int8, device=dev)
+wp = torch.zeros((256, 32), dtype=torch.uint8, device=dev)
+C = torch.empty((64, 256), dtype=torch.int32, device=dev)
+dY = torch.zeros((64, 256), dtype=torch.int8, device=dev)
+dW = torch.empty((128, 256), dtype=torch.float32, device=dev)
+torch.cuda.synchronize()
+free0 = torch.cuda.mem_get_info()[0]
+t3.t3_gemm_fwd(A, wp, K=128, C=C)
+t3.t3_gemm_bwd_dw_scaled(A, dY, None, None, t3.T3_OUT_F32, dW=dW)
+torch.cuda.synchronize()
+free1 = torch.cuda.mem_get_info()[0]
+t3.t3_gemm_bwd_dw_scaled_noalloc(A, dY, None, None, t3.T3_OUT_F32, dW=dW)
+torch.cuda.synchronize()
+free2 = torch.cuda.mem_get_info()[0]
+print(json.dumps({"other_calls": free0 - free1, "first_noalloc_call": free1 - free2}))
+"""
+
+
+@pytest.mark.gpu
+def test_noalloc_buffer_is_reserved_only_by_its_own_callers():
+    """In a fresh process with lazy module loading, the first fwd and scaled
+    dW calls (which use the same kernels as the no-alloc entry point) do not
+    reserve the fixed buffer's 32 MiB; the first no-alloc call does."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, CUDA_MODULE_LOADING="LAZY")
+    out = subprocess.run([sys.executable, "-c", _RESIDENCY_PROBE, root], env=env,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    got = json.loads(out.stdout.strip().splitlines()[-1])
+    mib = 1024 * 1024
+    assert got["other_calls"] < 32 * mib, got
+    assert got["first_noalloc_call"] >= 32 * mib, got
