@@ -97,10 +97,10 @@ int t3_pack_ternary_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N,
  *   A [M][K], Wp [N][ceil(K/4)], C [M][N] (layouts above), device pointers.
  * Exact for every input when K <= 16777215 (|A W| <= 128 K fits int32);
  * larger K returns T3_EOVERFLOW.  M <= 32 takes the small-M path, which is
- * bound by reading the packed weights: it enqueues two kernels on `stream`, one
- * that zeroes C and one that adds the product into it; the second may start
- * before the first ends (programmatic dependent launch) but touches C only
- * after it, and the first touches C only after all earlier work on `stream`.
+ * bound by reading the packed weights: it enqueues one kernel on `stream` as
+ * a programmatic dependent of the work before it, so that its launch and set-
+ * up overlap that work's end; it reads A and Wp and writes C only after all
+ * earlier work on `stream` has completed.
  * For M > 32, when whole output tiles would leave most of the GPU idle over a
  * long reduction (few tiles, many reduction stages) and A and Wp are
  * TMA-addressable, the reduction of the last tiles is split over the whole
@@ -126,8 +126,9 @@ int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, 
  * int8 x int8 products reach 16384, so the reduction is exact in int32 only
  * for M <= 131071 (the pages' bound); larger M returns T3_EOVERFLOW.
  * It enqueues two kernels on `stream`: one that zeroes dW and one that adds
- * 1024-row partial sums into it, with the same ordering as the small-M
- * forward above.
+ * 1024-row partial sums into it; the second may start before the first ends
+ * (programmatic dependent launch) but touches dW only after it, and the first
+ * touches dW only after all earlier work on `stream`.
  */
 int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N,
                    int64_t K, t3_stream_t stream);

@@ -34,14 +34,22 @@
 //     once, before the first unit;
 //   * the weights are decoded in registers straight into TMEM (the MMA's A
 //     operand), one byte permute per four weights, in a permuted order within
-//     each 16-code word (even codes, then odd codes) that the activations copy;
-//   * units are 128 weight rows x 512 k per CTA, ordered (tile, k) and split
-//     evenly over the pairs; each run of units of one tile ends with a TMA
-//     reduce-add of its int32 partial into C.  A small kernel zeroes C first.
-//     Both are launched as programmatic dependents: the zeroing kernel waits
-//     (griddepcontrol.wait) for the preceding grid to complete and then lets
-//     this kernel launch, whose prologue and weight stream overlap the
-//     zeroing; it waits for the zeroing only before its first reduce-add.
+//     each 16-code word (even codes, then odd codes) that the activations copy.
+// Schedule: a unit is 128 weight rows x 512 k per CTA.  A cluster of S CTA
+// pairs (S = 1 or 2, cluster of 2S CTAs) owns one 256-row tile at a time and
+// splits its reduction into S contiguous k-slices, one per pair; clusters take
+// tiles cluster, cluster + clusters, ...  Each pair sums its slice in TMEM
+// (runs of at most RUN_MAX units, added in int32 in shared memory), then the pairs
+// other than the first send their int32 partials into the first pair's shared
+// memory (st.async, counted on an mbarrier there), and the first pair adds
+// them and stores the tile.  Nothing is added into C in global memory, so C
+// needs no zeroing, no kernel runs before this one, and the result does not
+// depend on C's old contents.
+// Launch: the kernel is a programmatic dependent of whatever precedes it on
+// the stream and lets its own dependents launch at once, so a CTA that finds
+// an SM free sets up its barriers and TMEM before the preceding grid has
+// completed; it reads its inputs and writes C only after griddepcontrol.wait
+// (the preceding grid complete and its writes visible).
 #include <atomic>
 
 #include "t3.h"
@@ -61,10 +69,15 @@ constexpr int NB_MAX = 64;       // B rows (MMA N)
 constexpr int HALF_MAX = NB_MAX / 4;  // activation rows each CTA converts
 constexpr int TMEM_COLS = 512;
 constexpr int kMaxIssuers = 4;
+constexpr int kMaxSplit = 2;     // pairs per cluster (cluster of 4 CTAs)
 constexpr int ACC_REGION = 128;                  // kIss accumulators of 128 / kIss columns
 constexpr int kACol = ACC_REGION;                // then three weight buffers of 128 columns
 constexpr int kStepsPerUnit = UK / 32;           // MMA K-steps per unit
-constexpr int kDecWarps = 16;  // four per lane quadrant, each a quarter of every unit
+// Decoders: two groups of 8 warps take alternate units, so that one group's
+// per-unit waits and hand-offs overlap the other group's decode; in a group,
+// two warps per TMEM lane quadrant each decode half of every row.
+constexpr int kDecWarps = 16;
+constexpr int kGroupWarps = kDecWarps / 2;
 constexpr int kProducerWarp = kDecWarps;
 constexpr int kMmaWarp0 = kDecWarps + 1;  // MMA issuers (even CTA)
 constexpr int kEpiWarp0 = kMmaWarp0 + kMaxIssuers;
@@ -77,15 +90,20 @@ constexpr int ACT_BOX = 256;                      // activation bytes per TMA bo
 constexpr int ACT_BOX_BYTES = HALF_MAX * ACT_BOX;
 constexpr int RAW_ACT = (UK / ACT_BOX) * ACT_BOX_BYTES;  // [box][row][256 B]
 constexpr int RAW_STAGE = RAW_W + RAW_ACT;        // 24 KB
-constexpr int kActIters = HALF_MAX * (UK / 16) / (kDecWarps * 32);  // chunks per thread
+constexpr int kActIters = HALF_MAX * (UK / 16) / (kGroupWarps * 32);  // chunks per thread
 constexpr int B_ATOM = (NB_MAX / 2) * 128;   // one 128-k atom of up to NB/2 rows x 128 B
 constexpr int B_BUF = (UK / 128) * B_ATOM;   // 16 KB
 constexpr int STAGE_OUT = (NB_MAX / 2) * TN * 4;         // [NB/2 rows m][128 int32]
+// A partial of one CTA of a non-first pair: [up to 8 quads of m][128 n][4 m]
+// int32, so that the 16-byte accesses of consecutive n are consecutive.
+constexpr int SLOT_QUAD = TN * 16;
+constexpr int SLOT_BYTES = (NB_MAX / 8) * SLOT_QUAD;
 constexpr int OFF_RAW = 0;
 constexpr int OFF_B = OFF_RAW + RAW_STAGES * RAW_STAGE;
 constexpr int OFF_OUT = OFF_B + A_BUFS * B_BUF;
-constexpr int OFF_BAR = OFF_OUT + 2 * STAGE_OUT;
-constexpr int N_BARS = 2 * RAW_STAGES + 2 * A_BUFS + 2 + kMaxIssuers;
+constexpr int OFF_SLOT = OFF_OUT + STAGE_OUT;
+constexpr int OFF_BAR = OFF_SLOT + (kMaxSplit - 1) * SLOT_BYTES;
+constexpr int N_BARS = 2 * RAW_STAGES + 2 * A_BUFS + 2 + kMaxIssuers + 2;
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
 constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
 static_assert(RAW_STAGE % 1024 == 0, "swizzled TMA destinations need 1024-byte alignment");
@@ -96,30 +114,45 @@ static_assert(kStepsPerUnit % (4 * kMaxIssuers) == 0, "issuers split every unit 
 struct Params {
   const int8_t* A;     // [M][K]
   const uint8_t* Wp;   // [N][ceil(K/4)]
-  int32_t* C;          // [M][N], zeroed by the preceding kernel
+  int32_t* C;          // [M][N], overwritten
   int M, N, K;
   int NB;              // B rows = MMA N; NB/4 activation rows per CTA, NB/2 output rows m
+  int m4;              // output rows m sent between pairs: M rounded up to 4
   int ones_row;        // B row of ones (unsigned digits), or -1 (signed digits)
-  int units_total, units_k;  // units in (tile, k) order; units along k per tile
+  int tiles;           // pair tiles of 256 weight rows
+  int units_k;         // units along k per tile
+  int split;           // S: pairs per cluster, each a k-slice of upp units
+  int upp;             // units per pair slice: ceil(units_k / S)
   int use_tma_w, use_tma_out, use_tma_act;
   int* err;
 };
 
-// Walks units in (tile, k-unit) order.
+// Walks this pair's units: the tiles cid, cid + ncl, ... of its cluster, and
+// within each its k-slice [uk0, uk1).
 struct UnitIter {
-  int t, uk, units_k;
-  __device__ void init(const Params& p, int u) {
-    units_k = p.units_k;
-    t = u / units_k;
-    uk = u - t * units_k;
+  int t, uk, uk0, uk1, ncl;
+  __device__ void init(int cid, int ncl_, int uk0_, int uk1_) {
+    t = cid;
+    ncl = ncl_;
+    uk0 = uk0_;
+    uk1 = uk1_;
+    uk = uk0;
   }
+  __device__ bool tile_last() const { return uk + 1 == uk1; }
   __device__ void next() {
-    if (++uk == units_k) {
-      uk = 0;
-      ++t;
+    if (++uk == uk1) {
+      uk = uk0;
+      t += ncl;
     }
   }
 };
+
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                 "=r"(v[6]), "=r"(v[7])
+               : "r"(taddr));
+}
 
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
@@ -155,6 +188,16 @@ __device__ __forceinline__ void umma_f8_pair_ts(uint32_t d_tmem, uint32_t a_tmem
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on `bar` in both CTAs of the pair whose even CTA has cluster rank
+// `lead` once all prior MMAs of this thread are complete.
+__device__ __forceinline__ void umma_commit_to_pair(uint64_t* bar, uint32_t lead) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_addr(bar)),
+      "h"(static_cast<uint16_t>(0x3u << lead))
       : "memory");
 }
 
@@ -203,7 +246,7 @@ __device__ __forceinline__ void cluster_wait() {
 }
 
 template <bool kSigned, int kIss>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     skinny_fwd_kernel(const Params p, const __grid_constant__ CUtensorMap map_w,
                       const __grid_constant__ CUtensorMap map_out,
                       const __grid_constant__ CUtensorMap map_act) {
@@ -213,6 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* raw = smem + OFF_RAW;
   uint8_t* bop = smem + OFF_B;
   uint8_t* stage_out = smem + OFF_OUT;
+  uint8_t* slots = smem + OFF_SLOT;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* raw_full = bars;                    // TMA bytes landed
   uint64_t* raw_empty = raw_full + RAW_STAGES;  // decoders done with the stage
@@ -221,17 +265,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = a_empty + A_BUFS;        // both: run complete (multicast)
   uint64_t* acc_empty = acc_full + 1;           // even CTA: both epilogues drained
   uint64_t* drain_bar = acc_empty + 1;          // one per issuer, error path only
+  uint64_t* part_full = drain_bar + kMaxIssuers;  // first pair: the other pairs' partials in
+  uint64_t* slot_free = part_full + 1;          // other pairs: the first pair read the partials
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
   constexpr int kAccStride = ACC_REGION / kIss;  // columns per accumulator (>= NB)
   constexpr int kStepsPerIssuer = kStepsPerUnit / kIss;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = tc2::cluster_rank();
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int u0 = static_cast<int>(static_cast<int64_t>(p.units_total) * pair / npairs);
-  const int u1 = static_cast<int>(static_cast<int64_t>(p.units_total) * (pair + 1) / npairs);
-  const int n_units = u1 - u0;
+  const uint32_t crank = tc2::cluster_rank();     // 0 .. 2S - 1
+  const uint32_t rank = crank & 1u;               // CTA within the pair
+  const uint32_t lead = crank & ~1u;              // the pair's even CTA
+  const int qp = static_cast<int>(crank >> 1);    // pair within the cluster = k-slice
+  const int csize = 2 * p.split;
+  const int cid = blockIdx.x / csize, ncl = gridDim.x / csize;
+  const int uk0 = qp * p.upp;
+  const int uk1 = min(p.units_k, uk0 + p.upp);
+  const int my_tiles = cid < p.tiles ? (p.tiles - 1 - cid) / ncl + 1 : 0;
+  const int n_units = my_tiles * (uk1 - uk0);
   const int half_rows = p.NB >> 2;  // activation row slots of this CTA
   const int m_lo = static_cast<int>(rank) * half_rows;
   const int real_rows = max(0, min(p.M - m_lo, half_rows));  // activation rows present
@@ -245,15 +296,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RAW_STAGES; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], kDecWarps);
+      mbar_init(&raw_empty[s], kGroupWarps);
     }
     for (int s = 0; s < A_BUFS; ++s) {
-      mbar_init(&a_full[s], 2 * kDecWarps);  // the decoders of both CTAs
+      mbar_init(&a_full[s], 2 * kGroupWarps);  // one decoder group of each CTA
       mbar_init(&a_empty[s], kIss);
     }
     mbar_init(acc_full, kIss);
     mbar_init(acc_empty, 8);  // 4 epilogue warps x 2 CTAs
     for (int j = 0; j < kMaxIssuers; ++j) mbar_init(&drain_bar[j], 1);
+    mbar_init(part_full, 1);  // the first pair's arm (expect_tx) + the partials' bytes
+    mbar_init(slot_free, 1);  // one arrive of the first pair's CTA of the same rank
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -263,24 +316,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // Both CTAs' barriers and TMEM must exist before any remote arrive or pair
-  // MMA: every role waits on this cluster phase before its first such step;
-  // the producer, whose barriers are local, starts loading at once.
+  // Every CTA's barriers and TMEM must exist before any remote arrive, pair
+  // MMA or st.async: every role waits on this cluster phase before its first
+  // such step; the producer, whose barriers are local, starts loading at once.
   cluster_arrive_relaxed();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
   if (warp < kDecWarps) {
     // ------------------------------- weight decode -> TMEM, activations -> B
-    const int q = warp & 3, h = warp >> 2;  // lane quadrant, quarter of the unit
-    const int gtid = threadIdx.x;
+    const int grp = warp / kGroupWarps;          // units grp, grp + 2, ...
+    const int q = warp & 3, h = (warp >> 2) & 1;  // lane quadrant, half of every row
+    const int gtid = threadIdx.x - grp * kGroupWarps * 32;
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     // the even CTA's decoders arrive locally; the odd CTA's arrive on the even
     // CTA's barrier.  A signal-only arrive: the operands it announces stay in
     // this SM's TMEM and shared memory, already completed (tcgen05.wait::st)
     // and fenced for the tensor core (fence.proxy.async).
-    const uint32_t a_full_leader0 = tc2::peer_addr(&a_full[0], 0);
+    const uint32_t a_full_lead0 = tc2::peer_addr(&a_full[0], lead);
     // B rows that no activation row of this CTA rewrites: zero digits, and
     // the row of ones where it falls in this CTA
     const int dtid = threadIdx.x;  // 0 .. 32 * kDecWarps - 1
@@ -299,9 +353,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     named_bar_sync(kDecBarrier, 32 * kDecWarps);
     cluster_wait();
+    if (!p.use_tma_act) grid_dependency_wait();  // the activations are read with plain loads
     UnitIter it;
-    it.init(p, u0);
-    for (int i = 0; i < n_units; ++i, it.next()) {
+    it.init(cid, ncl, uk0, uk1);
+    if (grp == 1) it.next();
+    for (int i = grp; i < n_units; i += 2, it.next(), it.next()) {
       const int rs = i % RAW_STAGES, ab = i % A_BUFS;  // compile-time divisors
       const uint32_t rph = (i / RAW_STAGES) & 1, aph = (i / A_BUFS) & 1;
       bool ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2) &&
@@ -315,7 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint4 xa[kActIters];
 #pragma unroll
       for (int r = 0; r < kActIters; ++r) {
-        const int ci = gtid + r * kDecWarps * 32;
+        const int ci = gtid + r * kGroupWarps * 32;
         const int ml = ci / (UK / 16), c = ci % (UK / 16);
         xa[r] = make_uint4(0u, 0u, 0u, 0u);
         if (ci >= chunks) continue;
@@ -333,13 +389,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           xa[r] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      // 32 bytes = 128 codes of this row's quarter of the unit: 16-byte
-      // chunks 2h, 2h+1 of the row, in the 128-byte swizzle when TMA loaded them
+      // 64 bytes = 256 codes of this row's half of the unit, as two quarters
+      // of 128 codes (16-byte chunks 4h .. 4h+3 of the row, in the 128-byte
+      // swizzle when TMA loaded them), each decoded into 32 TMEM columns
       const uint8_t* src = stage + row * UB;
       const int swz = p.use_tma_w ? (row & 7) : 0;
-      const uint32_t col0 = kACol + ab * (UK / 4) + 32 * h;
-      {
-        const int c0 = 2 * h;
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        const int c0 = 4 * h + 2 * qq;
         const uint4 x0 = *reinterpret_cast<const uint4*>(src + ((c0 ^ swz) << 4));
         const uint4 x1 = *reinterpret_cast<const uint4*>(src + (((c0 + 1) ^ swz) << 4));
         uint32_t v[32];
@@ -351,14 +408,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         decode16_e4m3(x1.y, v + 20);
         decode16_e4m3(x1.z, v + 24);
         decode16_e4m3(x1.w, v + 28);
-        tc2::tmem_st_32x32b_x32(lane_addr + col0, v);
+        tc2::tmem_st_32x32b_x32(lane_addr + kACol + ab * (UK / 4) + 32 * (2 * h + qq), v);
       }
       // activations -> this CTA's half of the B operand: row 2 ml = hi
       // digits, row 2 ml + 1 = lo digits, atoms of 128 k in the 128-byte swizzle
       uint8_t* bbuf = bop + ab * B_BUF;
 #pragma unroll
       for (int r = 0; r < kActIters; ++r) {
-        const int ci = gtid + r * kDecWarps * 32;
+        const int ci = gtid + r * kGroupWarps * 32;
         if (ci >= chunks) continue;
         const int ml = ci / (UK / 16), c = ci % (UK / 16);
         uint4 hi, lo;
@@ -376,18 +433,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (rank == 0)
           mbar_arrive(&a_full[ab]);
         else
-          tc2::mbar_arrive_cluster_relaxed(a_full_leader0 + 8u * ab);
+          tc2::mbar_arrive_cluster_relaxed(a_full_lead0 + 8u * ab);
       }
     }
   } else if (warp == kProducerWarp) {
     // ------------------------------------- packed weights and activations in
+    const int64_t kbytes = (static_cast<int64_t>(p.K) + 3) / 4;
+    grid_dependency_wait();  // the inputs exist: the preceding grid has completed
     uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
     bool ok = true;
-    const int64_t kbytes = (static_cast<int64_t>(p.K) + 3) / 4;
     const uint32_t tx = (p.use_tma_w ? RAW_W : 0) +
                         (p.use_tma_act ? (UK / ACT_BOX) * half_rows * ACT_BOX : 0);
     UnitIter it;
-    it.init(p, u0);
+    it.init(cid, ncl, uk0, uk1);
     for (int i = 0; i < n_units; ++i, it.next()) {
       if (lane == 0)
         ok = mbar_wait(&raw_empty[stage], phase ^ 1u, abort_flag, p.err, code_base | 1);
@@ -436,13 +494,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true, issued_any = false, seg_first = true;
       int run_len = 0;
       UnitIter it;
-      it.init(p, u0);
+      it.init(cid, ncl, uk0, uk1);
       for (int i = 0; i < n_units; ++i, it.next()) {
         const int ab = i % A_BUFS;
         const uint32_t aph = (i / A_BUFS) & 1;
         ++run_len;
-        const bool seg_last =
-            (i + 1 == n_units) || (it.uk + 1 == it.units_k) || (run_len == RUN_MAX);
+        const bool seg_last = (i + 1 == n_units) || it.tile_last() || (run_len == RUN_MAX);
         if (seg_first) ok = mbar_wait(acc_empty, acc_ph ^ 1u, abort_flag, p.err, code_base | 3);
         if (ok) ok = mbar_wait(&a_full[ab], aph, abort_flag, p.err, code_base | 3);
         if (!ok) break;
@@ -460,10 +517,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                           bdesc0 + static_cast<uint64_t>(((s >> 2) * B_ATOM + 32 * (s & 3)) >> 4),
                           idesc, (seg_first && s == 0) ? 0u : 1u);
         issued_any = true;
-        tc2::umma_commit_pair(&a_empty[ab]);
+        umma_commit_to_pair(&a_empty[ab], lead);
         seg_first = seg_last;
         if (seg_last) {
-          tc2::umma_commit_pair(acc_full);
+          umma_commit_to_pair(acc_full, lead);
           run_len = 0;
           acc_ph ^= 1u;
         }
@@ -486,75 +543,74 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int etid = threadIdx.x - kEpiWarp0 * 32;
     const int nloc = q * 32 + lane;
-    const uint32_t acc_empty_leader0 = tc2::peer_addr(acc_empty, 0);
+    const uint32_t acc_empty_lead = tc2::peer_addr(acc_empty, lead);
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t acc_ph = 0, slab = 0;
+    const bool first_pair = qp == 0;
+    // a CTA of a later pair sends its partials to the first pair's CTA of the
+    // same rank (cluster rank `rank`), which holds the same weight rows
+    const uint32_t slot_remote =
+        first_pair ? 0u : tc2::peer_addr(slots + (qp - 1) * SLOT_BYTES + nloc * 16, rank);
+    const uint32_t part_full_remote = first_pair ? 0u : tc2::peer_addr(part_full, rank);
+    uint32_t acc_ph = 0, part_ph = 0, free_ph = 0;
     if (p.use_tma_out && etid == 0) prefetch_tensormap(&map_out);
     cluster_wait();
-    grid_dependency_wait();  // C has been zeroed (long before the first run ends)
+    grid_dependency_wait();  // C may be read by the preceding grid: write only after it
     UnitIter it;
-    it.init(p, u0);
-    int i = 0;
+    it.init(cid, ncl, uk0, uk1);
+    int i = 0, tile_count = 0;
+    bool run_first_of_tile = true;
+    // The tile's int32 partial of this CTA accumulates in the staging buffer
+    // [NB/2 rows m][128 n], each thread in its own column n (thread-private
+    // words, so no synchronisation between runs).
+    int32_t* sb = reinterpret_cast<int32_t*>(stage_out);
     while (i < n_units) {
       // the run of units of one tile that starts at unit i
       const int t = it.t;
       int len = 1;
-      while (i + len < n_units && it.uk + 1 < it.units_k && len < RUN_MAX) {
+      while (i + len < n_units && !it.tile_last() && len < RUN_MAX) {
         it.next();
         ++len;
       }
+      const bool tile_end = it.tile_last() || i + len == n_units;
       bool ok = mbar_wait(acc_full, acc_ph, abort_flag, p.err, code_base | 4);
       ok = named_bar_and(kEpiBarrier, 128, __all_sync(0xffffffffu, ok));
       if (!ok) break;
       tc_fence_after();
-      const int n0 = t * TP + static_cast<int>(rank) * TN;
-      const int64_t n = static_cast<int64_t>(n0) + nloc;
-      uint8_t* buf = stage_out + (slab & 1) * STAGE_OUT;
-      int32_t* sb = reinterpret_cast<int32_t*>(buf);
+      if (run_first_of_tile && p.use_tma_out && first_pair) {
+        // the previous tile's store has read the staging buffer
+        if (etid == 0) bulk_wait_group_read<0>();
+        named_bar_sync(kEpiBarrier, 128);
+      }
       // Summed over the issuers' accumulators, in units of 2^-9 (scaling by
       // 512 is exact): column 2m holds the hi digits' sum of row m, column
       // 2m + 1 the lo digits' sum, column ones_row the sum of the weights.
       int32_t bias = 0;  // 128 * sum_k w for unsigned digits
-      uint32_t o[kIss];
       if (!kSigned) {
+        uint32_t o[kIss];
 #pragma unroll
         for (int a = 0; a < kIss; ++a)
           asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
                        : "=r"(o[a]) : "r"(lane_base + a * kAccStride + p.ones_row));
+        tmem_wait_ld();
+        int32_t ones = 0;
+#pragma unroll
+        for (int a = 0; a < kIss; ++a) ones += __float2int_rn(__uint_as_float(o[a]) * 512.0f);
+        bias = 128 * ones;
       }
       // BW columns (BW/2 rows m) of every accumulator per TMEM round trip
-      constexpr int BW = 64 / kIss;
+      constexpr int BW = 32 / kIss;
       for (int cb = 0; cb < p.NB; cb += BW) {
         uint32_t d[kIss][BW];
-        const bool full = cb + BW <= p.NB;
 #pragma unroll
         for (int a = 0; a < kIss; ++a) {
-          if constexpr (BW == 32) {
-            if (full)
-              tmem_ld_32x32b_x32(lane_base + a * kAccStride + cb, d[a]);
-            else
-              tmem_ld_32x32b_x16(lane_base + a * kAccStride + cb,
-                                 *reinterpret_cast<uint32_t(*)[16]>(d[a]));
-          } else {
+          if constexpr (BW == 16)
             tmem_ld_32x32b_x16(lane_base + a * kAccStride + cb, d[a]);
-          }
+          else
+            tmem_ld_32x32b_x8(lane_base + a * kAccStride + cb, d[a]);
         }
         tmem_wait_ld();
-        if (cb == 0 && p.use_tma_out) {
-          // the staging buffer's previous bulk add has read it
-          if (etid == 0) bulk_wait_group_read<1>();
-          named_bar_sync(kEpiBarrier, 128);
-        }
-        if (!kSigned && cb == 0) {
-          int32_t ones = 0;
-#pragma unroll
-          for (int a = 0; a < kIss; ++a) ones += __float2int_rn(__uint_as_float(o[a]) * 512.0f);
-          bias = 128 * ones;
-        }
 #pragma unroll
         for (int e = 0; e < BW / 2; ++e) {
-          if (!full && e >= 8) break;
-          const int m = (cb >> 1) + e;
           int32_t hi = 0, lo = 0;
 #pragma unroll
           for (int a = 0; a < kIss; ++a) {
@@ -562,29 +618,78 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             lo += __float2int_rn(__uint_as_float(d[a][2 * e + 1]) * 512.0f);
           }
           const int32_t v = 16 * hi + lo - bias;
-          if (p.use_tma_out) {
-            sb[m * TN + nloc] = v;
-          } else if (n < p.N && m < p.M) {
-            atomicAdd(p.C + static_cast<int64_t>(m) * p.N + n, v);
-          }
+          int32_t* dst = sb + (cb / 2 + e) * TN + nloc;
+          *dst = run_first_of_tile ? v : *dst + v;
         }
       }
       tc_fence_before();
       __syncwarp();
       // the accumulator reads are complete (tcgen05.wait::ld): signal only
-      if (lane == 0) tc2::mbar_arrive_cluster_relaxed(acc_empty_leader0);
+      if (lane == 0) tc2::mbar_arrive_cluster_relaxed(acc_empty_lead);
       acc_ph ^= 1u;
+      run_first_of_tile = tile_end;
+      i += len;
+      if (i < n_units) it.next();
+      if (!tile_end) continue;
+      // ---- the tile's partial of this pair is complete in the staging buffer
+      if (!first_pair) {
+        // the first pair has read this CTA's previous partial
+        if (tile_count > 0) {
+          ok = mbar_wait(slot_free, free_ph, abort_flag, p.err, code_base | 4);
+          free_ph ^= 1u;
+          if (!__all_sync(0xffffffffu, ok)) break;
+        }
+        for (int e = 0; e < p.m4; e += 4)
+          st_async_v4(slot_remote + (e / 4) * SLOT_QUAD, sb[e * TN + nloc], sb[(e + 1) * TN + nloc],
+                      sb[(e + 2) * TN + nloc], sb[(e + 3) * TN + nloc], part_full_remote);
+        ++tile_count;
+        continue;
+      }
+      if (p.split > 1) {
+        if (etid == 0)
+          mbar_arrive_expect_tx(part_full, static_cast<uint32_t>((p.split - 1) * TN * p.m4 * 4));
+        ok = mbar_wait(part_full, part_ph, abort_flag, p.err, code_base | 4);
+        part_ph ^= 1u;
+        if (!named_bar_and(kEpiBarrier, 128, __all_sync(0xffffffffu, ok))) break;
+        for (int e = 0; e < p.m4; e += 4) {
+          int4 sum = make_int4(sb[e * TN + nloc], sb[(e + 1) * TN + nloc], sb[(e + 2) * TN + nloc],
+                               sb[(e + 3) * TN + nloc]);
+          for (int s = 1; s < p.split; ++s) {
+            const int4 x = *reinterpret_cast<const int4*>(slots + (s - 1) * SLOT_BYTES +
+                                                         (e / 4) * SLOT_QUAD + nloc * 16);
+            sum.x += x.x;
+            sum.y += x.y;
+            sum.z += x.z;
+            sum.w += x.w;
+          }
+          sb[e * TN + nloc] = sum.x;
+          sb[(e + 1) * TN + nloc] = sum.y;
+          sb[(e + 2) * TN + nloc] = sum.z;
+          sb[(e + 3) * TN + nloc] = sum.w;
+        }
+        // every partial has been read: the other pairs may send the next
+        // tile's (a cluster-scope release costs its thread about a microsecond,
+        // so only when the cluster has a next tile)
+        if (t + ncl < p.tiles) {
+          named_bar_sync(kEpiBarrier, 128);
+          if (etid == 0)
+            for (int s = 1; s < p.split; ++s)
+              tc2::mbar_arrive_cluster(tc2::peer_addr(slot_free, 2u * s + rank));
+        }
+      }
+      const int n0 = t * TP + static_cast<int>(rank) * TN;
+      const int64_t n = static_cast<int64_t>(n0) + nloc;
       if (p.use_tma_out) {
         fence_proxy_async_smem();
         named_bar_sync(kEpiBarrier, 128);
-        if (etid == 0 && n0 < p.N) {  // a tile half wholly past N adds nothing
-          tma_reduce_add_2d(&map_out, buf, n0, 0);
+        if (etid == 0 && n0 < p.N) {  // a tile half wholly past N stores nothing
+          tma_store_2d(&map_out, stage_out, n0, 0);
           bulk_commit_group();
         }
-        ++slab;
+      } else if (n < p.N) {
+        for (int e = 0; e < p.M; ++e) p.C[static_cast<int64_t>(e) * p.N + n] = sb[e * TN + nloc];
       }
-      i += len;
-      if (i < n_units) it.next();
+      ++tile_count;
     }
     if (p.use_tma_out && etid == 0) bulk_wait_group_read<0>();  // the stores finish by themselves
   }
@@ -592,8 +697,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   // No cross-CTA operation is in flight any more (the even CTA has seen the
-  // odd CTA's last arrive, the odd CTA the last commit); the barrier keeps
-  // the pair's TMEM allocated until both CTAs are done with it.
+  // odd CTA's last arrive, the odd CTA the last commit, the first pair every
+  // partial); the barrier keeps every CTA's shared memory and the pair's TMEM
+  // allocated until all CTAs of the cluster are done with them.
   cluster_arrive_relaxed();
   cluster_wait();
   tc_fence_after();
@@ -605,7 +711,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // Zeroes C ([n] int32).  Launched as a programmatic dependent of whatever
 // precedes it, so that its launch overlaps that grid's tail: it waits for that
-// grid to complete before anything else, then lets the product kernel launch.
+// grid to complete before anything else, then lets the next grid launch.
 __global__ void __launch_bounds__(256) zero_kernel_pdl(int32_t* C, int64_t n) {
   grid_dependency_wait();
   launch_dependents();
@@ -619,6 +725,38 @@ __global__ void __launch_bounds__(256) zero_kernel_pdl(int32_t* C, int64_t n) {
   } else {
     for (int64_t i = tid; i < n; i += stride) C[i] = 0;
   }
+}
+
+using KernelFn = void (*)(const Params, const CUtensorMap, const CUtensorMap, const CUtensorMap);
+
+// Kernel variant: signed digits for M = 32 (two issuers); four issuers while
+// each accumulator fits in 32 columns, else two.
+KernelFn pick_kernel(int M, int NB) {
+  if (M == 32) return skinny_fwd_kernel<true, 2>;
+  return NB <= 32 ? skinny_fwd_kernel<false, 4> : skinny_fwd_kernel<false, 2>;
+}
+
+// How many clusters of 2S CTAs can be resident at once (cached per device,
+// kernel variant and S).
+int max_clusters(int dev, int variant, int S, KernelFn fn) {
+  static std::atomic<int> cache[64][3][kMaxSplit + 1];
+  int v = cache[dev][variant][S].load(std::memory_order_acquire);
+  if (v > 0) return v;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2 * S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * S, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_ALLOC;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) return -1;
+  cache[dev][variant][S].store(n, std::memory_order_release);
+  return n;
 }
 
 }  // namespace sk
@@ -651,18 +789,22 @@ int launch_skinny_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M,
   p.K = static_cast<int>(K);
   const bool signed_digits = (M == 32);  // no spare B row for the ones
   p.NB = signed_digits ? 64 : static_cast<int>((2 * M + 1 + 15) / 16 * 16);
+  p.m4 = static_cast<int>((M + 3) / 4 * 4);
   p.ones_row = signed_digits ? -1 : static_cast<int>(2 * M);
-  p.units_k = static_cast<int>((K + sk::UK - 1) / sk::UK);
+  const int64_t units_k = (K + sk::UK - 1) / sk::UK;
   const int64_t tiles = (N + sk::TP - 1) / sk::TP;
-  const int64_t units = static_cast<int64_t>(p.units_k) * tiles;
-  if (units > 2147483647LL) return T3_EINVAL;
-  p.units_total = static_cast<int>(units);
+  if (tiles * units_k > 2147483647LL) return T3_EINVAL;
+  p.units_k = static_cast<int>(units_k);
+  p.tiles = static_cast<int>(tiles);
   p.err = err;
   const int64_t kbytes = (K + 3) / 4;
   CUtensorMap mw, mo, ma;
   p.use_tma_w = make_u8_map_tiled(&mw, Wp, N, kbytes, kbytes, sk::TN, sk::UB, true) ? 1 : 0;
   p.use_tma_act = make_u8_map_tiled(&ma, A, M, K, K, p.NB / 4, sk::ACT_BOX) ? 1 : 0;
   p.use_tma_out = make_i32_map_tiled(&mo, C, M, N, p.NB / 2, sk::TN, false) ? 1 : 0;
+  if (!p.use_tma_w) mw = p.use_tma_act ? ma : mo;  // unused copies: any initialised map
+  if (!p.use_tma_act) ma = mw;
+  if (!p.use_tma_out) mo = mw;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
@@ -681,28 +823,49 @@ int launch_skinny_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M,
       return T3_ECUDA;
     attr_done[dev].store(true, std::memory_order_release);
   }
+  const sk::KernelFn fn = sk::pick_kernel(p.M, p.NB);
+  const int variant = signed_digits ? 2 : (p.NB <= 32 ? 0 : 1);
 
-  const int zst = launch_zero_pdl(C, M * N, sms, s);
-  if (zst != T3_OK) return zst;
-  cudaLaunchAttribute attr[1];
+  // Split: S pairs per cluster share a tile's reduction.  Estimated time in
+  // units of one pair's unit: waves of tiles x units per slice, plus about one
+  // unit for the partials' exchange when S > 1.  Every pair needs a nonempty
+  // slice.  Ties go to the smaller cluster.
+  int best_s = 1, best_clusters = 1;
+  int64_t best_cost = -1;
+  for (int S = 1; S <= sk::kMaxSplit; ++S) {
+    const int64_t upp = (units_k + S - 1) / S;
+    if (S > units_k || (S - 1) * upp >= units_k) continue;
+    const int mc = sk::max_clusters(dev, variant, S, fn);
+    if (mc < 1) continue;
+    const int64_t ncl = tiles < mc ? tiles : mc;
+    const int64_t waves = (tiles + ncl - 1) / ncl;
+    const int64_t cost = waves * upp + (S > 1 ? 1 : 0);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_s = S;
+      best_clusters = static_cast<int>(ncl);
+    }
+  }
+  if (best_cost < 0) return T3_ECUDA;  // no cluster shape can be resident
+  p.split = best_s;
+  p.upp = static_cast<int>((units_k + best_s - 1) / best_s);
+
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-
-  const int64_t max_pairs = sms / 2 > 0 ? sms / 2 : 1;
-  const int npairs = static_cast<int>(units < max_pairs ? units : max_pairs);
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2 * best_s;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * npairs, 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * best_s * best_clusters), 1, 1);
   cfg.blockDim = dim3(sk::kThreads, 1, 1);
   cfg.dynamicSmemBytes = sk::SMEM_ALLOC;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // four issuers while each accumulator fits in 32 columns, else two
-  const cudaError_t le =
-      signed_digits ? cudaLaunchKernelEx(&cfg, sk::skinny_fwd_kernel<true, 2>, p, mw, mo, ma)
-      : p.NB <= 32  ? cudaLaunchKernelEx(&cfg, sk::skinny_fwd_kernel<false, 4>, p, mw, mo, ma)
-                    : cudaLaunchKernelEx(&cfg, sk::skinny_fwd_kernel<false, 2>, p, mw, mo, ma);
-  if (le != cudaSuccess) return T3_ECUDA;
+  cfg.numAttrs = 2;
+  (void)sms;
+  if (cudaLaunchKernelEx(&cfg, fn, p, mw, mo, ma) != cudaSuccess) return T3_ECUDA;
   return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
 }
 

@@ -169,3 +169,58 @@ def test_dw_chunk_limit_both_signs():
     got = dW.cpu().numpy()
     bad = np.argwhere(got != want)
     assert bad.size == 0, f"dW chunk limit: {len(bad)} mismatches; first {bad[0].tolist()}"
+
+
+# ------------------------------------------------------------------ small M
+# The small-M forward multiplies e4m3 weights (+-1) by activation digits in
+# e4m3 (bytes 0..15, each exactly byte * 2^-9) and sums in f32 in TMEM, one
+# accumulator per issuing thread, over runs of up to 2048 units of 512
+# reduction elements: an accumulator adds at most 2048 * 512 / issuers terms
+# of magnitude <= 15 (units of 2^-9), 7.9 M units with two issuers, inside
+# 2^24.  K = 4 * 2048 * 512 over one 256-row tile gives each of the two CTA
+# pairs that share the tile a slice of exactly two full runs.  Digits of 15
+# (a = 127: u = a + 128 = 255; or a = -128 for the signed digits of M = 32)
+# fill the accumulators for all but the last unit of every run, whose terms
+# are digits 0 or 1 times weights -1, 0 or +1.
+
+SLICE = 2048 * 512
+K_SMALL_M = 4 * SLICE
+
+
+def small_m_rows(g, signed):
+    """4 row classes of length K_SMALL_M (see the module comment above)."""
+    rows = np.empty((4, K_SMALL_M), dtype=np.int8)
+    if signed:
+        small_vals = np.array([1, 16, -16, 0, -1], dtype=np.int8)   # hi/lo digits 0 or +-1
+        big = (127, -128, 127)
+    else:
+        small_vals = np.array([-127, -112, -128], dtype=np.int8)   # u = 1, 16, 0
+        big = (127, 127, 127)
+    rows[0] = big[0]
+    rows[1] = big[1]
+    rows[2] = t3_synth.int8_uniform(g, K_SMALL_M)
+    rows[3] = big[2]
+    rows[3].reshape(-1, 512)[1::2] = small_vals[-1]          # every other unit: small values
+    for r in (0, 1, 3):
+        for q in range(4):
+            end = (q + 1) * SLICE
+            rows[r, end - 512:end] = g.choice(small_vals, size=512)
+    return rows
+
+
+@pytest.mark.parametrize("M", [1, 8, 31, 32])
+def test_small_m_run_limit(M):
+    g = t3_synth.rng(4 * SLICE + M)
+    N = 256
+    classes = small_m_rows(g, signed=(M == 32))
+    cls = (np.arange(M) * 3 + np.arange(M) // 4) % 4
+    A = np.ascontiguousarray(classes[cls])
+    # weights +1 (code 1, byte 0x55) except random codes in the last unit of every slice
+    wp = np.full((N, K_SMALL_M // 4), 0x55, dtype=np.uint8)
+    for q in range(4):
+        end = (q + 1) * SLICE // 4
+        wp[:, end - 128:end] = t3_synth.raw_bytes(g, (N, 128))
+    C = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    t3.t3_gemm_fwd(torch.from_numpy(A).cuda(), torch.from_numpy(wp).cuda(), K=K_SMALL_M, C=C)
+    want = oracle.fwd(classes, wp)
+    expand_and_check(C.cpu().numpy(), cls, want, f"small-M run limit M={M}")

@@ -248,6 +248,37 @@ def test_small_m_boundaries(M):
         assert_same(run_fwd(A, wp), oracle.fwd(A, oracle.pack(w)), f"fwd {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (8, 10240, 8192),    # 40 tiles of 256 rows: clusters of up to 4 CTA pairs, several tiles each
+    (32, 10240, 8192),
+    (27, 24576, 8192),   # 96 tiles: clusters of 2 pairs, three tiles each
+    (1, 24576, 4100),    # ragged last unit, packed rows not 16-byte aligned
+    (16, 3456 * 3, 1280),
+    (5, 300, 70000),     # one tile, a long reduction split over the cluster's pairs
+])
+def test_small_m_cluster_schedules(M, N, K):
+    """Small-M shapes whose tiles and k-slices exercise every cluster shape
+    of the small-M path: one tile per cluster or several (the first pair's
+    partial buffers reused), one to four pairs per cluster."""
+    A, w, _ = inputs(M, N, K, seed=M + N + K)
+    wp = oracle.pack(w)
+    assert_same(run_fwd(A, wp), oracle.fwd(A, wp), f"fwd {M}x{N}x{K}")
+
+
+def test_small_m_output_not_zeroed_first():
+    """The small-M path overwrites C without reading it: garbage in C before
+    the call (and a previous product's result) leaves no trace."""
+    g = t3_synth.rng(404)
+    for (M, N, K) in [(8, 1024, 4096), (27, 3456, 1280)]:
+        A = t3_synth.int8_uniform(g, (M, K))
+        wp = oracle.pack(t3_synth.ternary(g, (K, N)))
+        C = torch.randint(-2**31, 2**31 - 1, (M, N), dtype=torch.int32, device="cuda")
+        t3.t3_gemm_fwd(_dev(A), _dev(wp), K=K, C=C)
+        t3.t3_gemm_fwd(_dev(A), _dev(wp), K=K, C=C)
+        torch.cuda.synchronize()
+        assert_same(C.cpu().numpy(), oracle.fwd(A, wp), f"fwd {M}x{N}x{K} over garbage")
+
+
 def test_small_m_extremes():
     K = 8192
     for M in (1, 27):
