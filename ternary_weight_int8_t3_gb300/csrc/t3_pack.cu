@@ -12,13 +12,23 @@
 // the instruction count per weight low.  A CTA takes a tile of 64 k x 256 n: it
 // reads the tile's 64 rows with coalesced loads (16 bytes per thread where
 // every row is 16-byte aligned, single bytes otherwise) into shared memory.
-// Each thread then owns 4 columns x 16 k: per 4 rows it reads four 32-bit
-// words (64 threads read a row's 256 bytes, conflict-free), transposes the
-// 4 x 4 bytes with byte permutes so that each word holds 4 k of one column,
-// and turns that word into one packed byte with a few bitwise operations
-// (SWAR), checking the four values at once.  The packed words are staged in
+// Each thread then owns 4 columns x 16 k: it reads one 32-bit word per row
+// (64 threads read a row's 256 bytes, conflict-free), turns each word into
+// the four columns' 2-bit codes with a few bitwise operations (SWAR), which
+// also check the four values at once, ORs the codes of 4 rows into one word
+// of 4 packed bytes, and transposes the resulting 4 x 4 bytes once.  The packed words are staged in
 // shared memory so that each column's 16 packed bytes leave as one 16-byte
 // store.
+//
+// Where w can be a TMA source (rows of a multiple of 16 bytes, 16-byte aligned
+// base), one CTA per SM walks the tiles with the loads decoupled from the
+// packing: a producer warp streams them by TMA into a ring of eight stages
+// (~128 KB per SM in flight), and three groups of eight warps pack the tiles
+// in turn with the same per-thread work as above.  Tiles past K or N arrive
+// zero-filled (code 0, as the pad positions want).  (Tiles of two stages, so
+// that each column's packed bytes fill a 32-byte sector of Wp, measured no
+// faster.)
+#include <atomic>
 #include <cstdint>
 
 #include "t3.h"
@@ -38,26 +48,50 @@ __device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t s
   return r;
 }
 
-// Four int8 weights (one per byte) -> their four 2-bit codes in one byte
-// (byte j's code at bits 2j); a byte other than 0x00, 0x01, 0xFF packs as
-// code 0 and sets `bad`.
-__device__ __forceinline__ uint32_t pack4(uint32_t x, bool& bad) {
-  // bytewise x + 1 (no carries between bytes): valid bytes become 0, 1 or 2,
-  // i.e. bits 2-7 clear and not both bits 0 and 1 set
-  const uint32_t inc = ((x & 0x7F7F7F7Fu) + 0x01010101u) ^ (x & 0x80808080u);
-  if (((inc & 0xFCFCFCFCu) | (inc & (inc >> 1) & 0x01010101u)) != 0u) {
-    bad = true;  // rare: byte by byte, invalid bytes as code 0
-    uint32_t r = 0u;
+// The 2-bit codes of four int8 weights (one per byte), each in the low bits
+// of its byte: +1 -> 1, -1 -> 2, 0 -> 0.  Per byte, lo = bit 0 and sg = the
+// sign bit; the valid bytes are exactly the ones rebuilt by lo | (sg ? 0xFF :
+// 0) -- 0x00, 0x01 and 0xFF (sg * 0xFF stays inside its byte) -- and their
+// codes are lo + sg.  A word with another byte takes the byte-by-byte path
+// (rare): invalid bytes get code 0 and set `bad`.
+__device__ __forceinline__ uint32_t codes4(uint32_t x, bool& bad) {
+  const uint32_t lo = x & 0x01010101u, sg = (x >> 7) & 0x01010101u;
+  if ((lo | (sg * 0xFFu)) == x) return lo + sg;
+  bad = true;
+  uint32_t r = 0u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int v = static_cast<int8_t>(x >> (8 * j));
-      r |= (v == 1 ? 1u : (v == -1 ? 2u : 0u)) << (2 * j);
-    }
-    return r;
+  for (int j = 0; j < 4; ++j) {
+    const int v = static_cast<int8_t>(x >> (8 * j));
+    r |= (v == 1 ? 1u : (v == -1 ? 2u : 0u)) << (8 * j);
   }
-  const uint32_t b0 = x & 0x01010101u, b1 = (x >> 1) & 0x01010101u;
-  const uint32_t c = (b0 & ~b1) | (b1 << 1);  // +1 -> 1, -1 -> 2, 0 -> 0, per byte
-  return (c | (c >> 6) | (c >> 12) | (c >> 18)) & 0xFFu;
+  return r;
+}
+
+// The packing of one [TK][TN] tile by one thread: columns 4 cg .. 4 cg + 3,
+// k rows 16 kq .. 16 kq + 15.  A row's word holds the four columns' weights
+// at one k; the code words of four consecutive rows, shifted by 0, 2, 4 and
+// 6 bits, OR into one word whose byte i is column i's packed byte for those
+// four k (codes fill 2 bits, so nothing crosses into the next byte).  A 4 x 4
+// byte transpose of the four such words gives out[i], column i's 4 packed
+// bytes (16 k).
+__device__ __forceinline__ void pack_tile(const int8_t (*tile)[TN], int cg, int kq,
+                                          uint32_t (&out)[4], bool& bad) {
+  uint32_t q[4];
+#pragma unroll
+  for (int sb = 0; sb < 4; ++sb) {
+    const int r = 16 * kq + 4 * sb;
+    uint32_t word = 0u;
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr)
+      word |= codes4(*reinterpret_cast<const uint32_t*>(&tile[r + rr][4 * cg]), bad) << (2 * rr);
+    q[sb] = word;
+  }
+  const uint32_t a = byte_perm(q[0], q[1], 0x5140u), b = byte_perm(q[2], q[3], 0x5140u);
+  const uint32_t c = byte_perm(q[0], q[1], 0x7362u), d = byte_perm(q[2], q[3], 0x7362u);
+  out[0] = byte_perm(a, b, 0x5410u);
+  out[1] = byte_perm(a, b, 0x7632u);
+  out[2] = byte_perm(c, d, 0x5410u);
+  out[3] = byte_perm(c, d, 0x7632u);
 }
 
 // Tiles are numbered n-block fastest and walked grid-stride.
@@ -97,22 +131,8 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const int8_t* __restrict
     }
     __syncthreads();
     // rows past K hold 0 and pack as code 0
-    uint32_t out[4] = {0u, 0u, 0u, 0u};  // per column: 4 packed bytes = 16 k
-#pragma unroll
-    for (int sb = 0; sb < 4; ++sb) {
-      const int r = 16 * kq + 4 * sb;
-      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(&tile[r][4 * cg]);
-      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(&tile[r + 1][4 * cg]);
-      const uint32_t w2 = *reinterpret_cast<const uint32_t*>(&tile[r + 2][4 * cg]);
-      const uint32_t w3 = *reinterpret_cast<const uint32_t*>(&tile[r + 3][4 * cg]);
-      // 4 x 4 byte transpose: col[i] = byte i of w0, w1, w2, w3 (4 k of column i)
-      const uint32_t a = byte_perm(w0, w1, 0x5140u), b = byte_perm(w2, w3, 0x5140u);
-      const uint32_t c = byte_perm(w0, w1, 0x7362u), d = byte_perm(w2, w3, 0x7362u);
-      const uint32_t col[4] = {byte_perm(a, b, 0x5410u), byte_perm(a, b, 0x7632u),
-                               byte_perm(c, d, 0x5410u), byte_perm(c, d, 0x7632u)};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) out[i] |= pack4(col[i], bad) << (8 * sb);
-    }
+    uint32_t out[4];  // per column: 4 packed bytes = 16 k
+    pack_tile(tile, cg, kq, out, bad);
 #pragma unroll
     for (int i = 0; i < 4; ++i) packed[4 * cg + i][kq] = out[i];
     __syncthreads();
@@ -135,6 +155,109 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const int8_t* __restrict
   if (__any_sync(0xffffffffu, bad) && (t & 31) == 0) atomicCAS(err, 0, kErrInvalid);
 }
 
+constexpr int kStages = 8;
+constexpr int kGroups = 3;                          // consumer groups, tiles in turn
+constexpr int kSub = 1;                             // 64-row ring stages per tile
+constexpr int kTmaThreads = kGroups * kThreads + 32;  // + the producer warp
+constexpr int kTileBytes = TK * TN;
+constexpr int kTmaSmem = kStages * kTileBytes + 128;
+constexpr int kRowWords = 4 * kSub;                 // packed words per column per tile
+static_assert(kGroups * kSub <= kStages, "every group can hold its tile's stages");
+
+// Tiles of kSub * 64 k x 256 n, numbered n-block fastest; each column of a
+// tile makes kSub * 16 packed bytes of its Wp row.
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    pack_tma_kernel(const __grid_constant__ CUtensorMap map_w, uint8_t* __restrict__ wp,
+                    int64_t N, int64_t KB, int64_t tiles_n, int64_t tiles, int vec_out,
+                    int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  int8_t (*ring)[TK][TN] = reinterpret_cast<int8_t (*)[TK][TN]>(
+      smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u));
+  // a group's packed rows, padded by one word so that the 4-byte stores of
+  // consecutive column groups spread over the banks
+  __shared__ uint32_t packed[kGroups][TN][kRowWords + 1];
+  __shared__ uint64_t full[kStages], empty[kStages];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kThreads / 32);  // the warps of the group that packed the stage
+    }
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  const int64_t my_tiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  constexpr int code = (9 << 8) | 1;
+  if (warp == kGroups * (kThreads / 32)) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_w);
+      for (int64_t j = 0; j < my_tiles * kSub; ++j) {  // ring stage j: part j % kSub of a tile
+        const int s = static_cast<int>(j % kStages);
+        if (!mbar_wait(&empty[s], static_cast<uint32_t>((j / kStages) & 1) ^ 1u, &abort_flag, err,
+                       code))
+          break;
+        const int64_t tix = blockIdx.x + (j / kSub) * gridDim.x;
+        const int64_t tk = tix / tiles_n;
+        mbar_arrive_expect_tx(&full[s], kTileBytes);
+        tma_load_2d(ring[s], &map_w, &full[s], static_cast<int32_t>((tix - tk * tiles_n) * TN),
+                    static_cast<int32_t>(tk * TK * kSub + (j % kSub) * TK));
+      }
+    }
+    return;
+  }
+  // ------------------------------------------------------------- consumers
+  const int grp = warp / (kThreads / 32);
+  const int t = threadIdx.x - grp * kThreads;
+  const int cg = t % (TN / 4), kq = t / (TN / 4);
+  bool bad = false;
+  for (int64_t i = grp; i < my_tiles; i += kGroups) {
+    uint32_t out[kSub][4];
+    bool ok = true;
+#pragma unroll
+    for (int h = 0; h < kSub; ++h) {
+      const int64_t j = i * kSub + h;
+      const int s = static_cast<int>(j % kStages);
+      ok = mbar_wait(&full[s], static_cast<uint32_t>((j / kStages) & 1), &abort_flag, err,
+                     code + 1);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      pack_tile(ring[s], cg, kq, out[h], bad);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const int64_t tix = blockIdx.x + i * gridDim.x;
+    const int64_t tk = tix / tiles_n;
+    const int64_t n0 = (tix - tk * tiles_n) * TN;
+    named_bar_sync(1 + grp, kThreads);  // this group's previous packed rows are stored
+#pragma unroll
+    for (int h = 0; h < kSub; ++h)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) packed[grp][4 * cg + c][4 * h + kq] = out[h][c];
+    named_bar_sync(1 + grp, kThreads);
+    const int64_t n = n0 + t;
+    const int64_t b0 = tk * (kSub * TK / 4);
+    if (n < N) {
+      uint8_t* dst = wp + n * KB + b0;
+      const uint32_t* row = packed[grp][t];
+#pragma unroll
+      for (int h = 0; h < kSub; ++h) {
+        const int64_t off = b0 + 16 * h;
+        if (vec_out && off + 16 <= KB) {
+          *reinterpret_cast<uint4*>(dst + 16 * h) =
+              make_uint4(row[4 * h], row[4 * h + 1], row[4 * h + 2], row[4 * h + 3]);
+        } else {
+          for (int b = 0; b < 16 && off + b < KB; ++b)
+            dst[16 * h + b] = static_cast<uint8_t>(row[4 * h + (b >> 2)] >> (8 * (b & 3)));
+        }
+      }
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicCAS(err, 0, kErrInvalid);
+}
+
 }  // namespace pack
 
 int launch_pack_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N, int sms, int* err,
@@ -144,6 +267,25 @@ int launch_pack_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N, int s
   const int64_t tiles = tiles_n * tiles_k;
   const int vec_in = (N % 16 == 0) && (reinterpret_cast<uintptr_t>(w) % 16 == 0);
   const int vec_out = (KB % 16 == 0) && (reinterpret_cast<uintptr_t>(wp) % 16 == 0);
+  CUtensorMap map;
+  if (vec_in && make_u8_map_tiled(&map, w, K, N, N, pack::TK, pack::TN, false)) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
+    static std::atomic<bool> attr_done[64];
+    if (dev < 0 || dev >= 64) return T3_EDEVICE;
+    if (!attr_done[dev].load(std::memory_order_acquire)) {
+      if (cudaFuncSetAttribute(pack::pack_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               pack::kTmaSmem) != cudaSuccess)
+        return T3_ECUDA;
+      attr_done[dev].store(true, std::memory_order_release);
+    }
+    const int64_t tiles_k2 = (K + pack::kSub * pack::TK - 1) / (pack::kSub * pack::TK);
+    const int64_t tiles2 = tiles_n * tiles_k2;
+    const int64_t grid = tiles2 < sms ? tiles2 : sms;
+    pack::pack_tma_kernel<<<static_cast<unsigned>(grid > 0 ? grid : 1), pack::kTmaThreads,
+                            pack::kTmaSmem, s>>>(map, wp, N, KB, tiles_n, tiles2, vec_out, err);
+    return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
+  }
   // enough CTAs to keep every SM's loads in flight, each walking several tiles
   const int64_t cap = 16 * static_cast<int64_t>(sms > 0 ? sms : 1);
   const int64_t grid = tiles < cap ? tiles : cap;

@@ -1,8 +1,9 @@
 """GPU parity of the device packer (t3_pack_ternary_device) against the oracle's
 packer, byte for byte, through the C ABI.
 
-Covers the tile edges (K and N not multiples of the 64 x 128 tile, K not a
-multiple of 4), both load paths (16-byte rows and unaligned rows), both store
+Covers the tile edges (K and N not multiples of the 64 x 256 tile, K not a
+multiple of 4), both load paths (TMA for 16-byte rows, plain loads for
+unaligned rows), both store
 paths (8-byte words and single bytes), canaries around the output, invalid
 values (packed as 0 and reported as T3_EVALUE), and a packed result feeding
 the forward product.
@@ -48,8 +49,11 @@ def _device_pack(w, w_offset=0, wp_offset=0):
     return wp.cpu().numpy()
 
 
+# rows of w that are a multiple of 16 bytes take the TMA-fed kernel (tiles of
+# 64 k x 256 n, zero-filled past K and N), the others the plain-load one
 SHAPES = [(1, 1), (3, 5), (4, 16), (5, 7), (63, 127), (64, 128), (65, 129), (96, 272),
-          (1000, 333), (130, 4096), (1280, 3456)]
+          (1000, 333), (130, 4096), (1280, 3456), (13, 64), (257, 1024), (8191, 16),
+          (4100, 2048)]
 
 
 @pytest.mark.parametrize("K,N", SHAPES)
@@ -72,8 +76,9 @@ def test_device_pack_all_zero_and_all_ones():
         np.testing.assert_array_equal(_device_pack(w), oracle.pack(w))
 
 
-def test_device_pack_invalid_values_pack_as_zero_and_are_reported():
-    K, N = 200, 300
+@pytest.mark.parametrize("N", [300, 320])
+def test_device_pack_invalid_values_pack_as_zero_and_are_reported(N):
+    K = 200
     w = t3_synth.ternary(t3_synth.rng(77), (K, N))
     bad = [(0, 0, 2), (17, 5, -2), (199, 299, 127), (64, 128, -128), (3, 150, 100)]
     for k, n, v in bad:
