@@ -362,6 +362,44 @@ def bench_quantize(t3, torch, dev, stream, hbm_gbs, M, K, reps=20):
             "frac_hbm": round(gbs / hbm_gbs, 3), "timing": "graph"}
 
 
+def bench_fused_quant(t3, torch, dev, stream, wp_d, reps=10):
+    """The row quantizer and the forward at the layer shape, two ways: the
+    quantizer kernel and then the forward on its int8 output (two passes over
+    the bf16 activations, int8 written and read back), and the quantizer fused
+    into the forward (a scales-only pass, then the forward's converters
+    quantize the bf16 tiles).  bf16 inputs rotate past the L2."""
+    g = torch.Generator(device="cpu").manual_seed(11)
+    x = (torch.randn((M, K), generator=g) * 3).to(torch.bfloat16).to(dev)
+    copies = max(2, -(-2 * 129 * 2**20 // (x.numel() * 2)))
+    xs = [x.clone() for _ in range(copies)]
+    q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    sc = torch.empty((M,), dtype=torch.float32, device=dev)
+    inv = torch.empty((M,), dtype=torch.float32, device=dev)
+    C = torch.empty((M, N), dtype=torch.int32, device=dev)
+
+    def unfused(i):
+        t3.t3_quantize_rows_bf16(xs[i % copies], q, sc, stream=stream)
+        t3.t3_gemm_fwd(q, wp_d, K=K, C=C, stream=stream)
+
+    def fused(i):
+        t3.t3_gemm_fwd_bf16(xs[i % copies], wp_d, C=C, row_scale=sc, row_inv=inv, stream=stream)
+
+    out = {}
+    for name, call in (("quantize_then_fwd", unfused), ("fused_fwd_bf16", fused)):
+        for i in range(3):
+            call(i)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            call(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        out[name] = {"us": round(us, 1), "TOPS": round(OPS_PER_PRODUCT / (us * 1e-6) / 1e12, 1)}
+    return out
+
+
 def bench_configs(t3, torch, dev, stream, peak, reps=20):
     """The other full-size workloads, each product timed on its own: the
     square forward 4096^3 (weights P(0) = 1/2) and the backward of the pages'
@@ -695,6 +733,7 @@ def main():
     if not args.step_only:
         line["scaled_f32"] = bench_scaled(t3, torch, dev, stream, A_d, wp_d, dY_d, K)
         line["quantize_rows"] = bench_quantize(t3, torch, dev, stream, hbm, M, K)
+        line["quantized_fwd_bf16"] = bench_fused_quant(t3, torch, dev, stream, wp_d)
     if not args.step_only:
         line["configs"] = bench_configs(t3, torch, dev, stream, peak)
     if not (args.no_pack or args.step_only):

@@ -152,6 +152,28 @@ int t3_quantize_rows_bf16(const void* x, int8_t* q, float* row_scale, int64_t M,
                           t3_stream_t stream);
 
 /*
+ * t3_gemm_fwd_bf16 -- the row quantizer fused into the forward product: the
+ * same result as t3_quantize_rows_bf16(X, q, row_scale) followed by
+ * t3_gemm_fwd(q, Wp, C), without writing q.  A first kernel takes each row's
+ * absolute maximum and writes
+ *   row_scale[m] = amax / 127 and row_inv[m] = 127 / amax   (0 and 0 for a
+ *   zero row; the divisions of t3_quantize_rows_bf16),
+ * then the forward pair pipeline reads X as bf16 tiles and its converters
+ * quantize them (q = rint(x * row_inv[m]), ties to even) on their way to the
+ * tensor core:
+ *   C[m][n] = sum_k q[m][k] * W[k][n]     (exact int32, as t3_gemm_fwd).
+ *   X DEVICE bf16 [M][K] (bit patterns), Wp DEVICE [N][ceil(K/4)], C DEVICE
+ *   int32 [M][N], row_scale and row_inv DEVICE float [M]; caller-owned.
+ * The fused kernel takes M > 32, K a multiple of 64 and X, Wp 16-byte aligned
+ * (bf16 and packed rows TMA can address); any other shape returns T3_EINVAL
+ * without launching (quantize, then multiply, instead).  N = 0 computes the
+ * scales only; K = 0 writes zero scales and a zero C.  Asynchronous on
+ * `stream`.  Finite inputs, as for t3_quantize_rows_bf16.
+ */
+int t3_gemm_fwd_bf16(const void* X, const uint8_t* Wp, int32_t* C, float* row_scale,
+                     float* row_inv, int64_t M, int64_t N, int64_t K, t3_stream_t stream);
+
+/*
  * Scaled outputs -- the step after the products in "spec(igla): hslm_bwd_ptx
  * -- HSLM backward dX and dW as int8 tensor-core PTX written by t27": the
  * host rescales the integer results (dX by a scale per row; dW by scales per

@@ -12,6 +12,7 @@ Function names follow the C ABI:
   t3_gemm_bwd_dx(dY, Wp, K, dX=None)       dX = dY . W^T     (int32 [M][K])
   t3_gemm_bwd_dw(A, dY, dW=None)           dW = A^T . dY     (int32 [K][N])
   t3_quantize_rows_bf16(x)                 (int8 q, per-row scale) from bf16 x
+  t3_gemm_fwd_bf16(x, Wp)                  the quantizer fused into the forward
   t3_dequant_i32(x, kind, row_scale, col_scale, out=None)   scaled float/bf16 output
   t3_gemm_fwd_scaled / t3_gemm_bwd_dx_scaled / t3_gemm_bwd_dw_scaled
                                            the products with that output
@@ -69,6 +70,8 @@ def load():
         lib.t3_pack_ternary_device.restype = ctypes.c_int
         lib.t3_quantize_rows_bf16.argtypes = [p, p, p, i64, i64, p]
         lib.t3_quantize_rows_bf16.restype = ctypes.c_int
+        lib.t3_gemm_fwd_bf16.argtypes = [p, p, p, p, p, i64, i64, i64, p]
+        lib.t3_gemm_fwd_bf16.restype = ctypes.c_int
         lib.t3_dequant_i32.argtypes = [p, p, i64, i64, p, p, ctypes.c_int, p]
         lib.t3_dequant_i32.restype = ctypes.c_int
         for name in ("t3_gemm_fwd_scaled", "t3_gemm_bwd_dx_scaled", "t3_gemm_bwd_dw_scaled"):
@@ -277,6 +280,34 @@ def t3_quantize_rows_bf16(x, q=None, row_scale=None, stream=None):
         rc = load().t3_quantize_rows_bf16(*args)
     _check(rc, "t3_quantize_rows_bf16")
     return q, row_scale
+
+
+def t3_gemm_fwd_bf16(x, Wp, C=None, row_scale=None, row_inv=None, stream=None):
+    """(C, row_scale, row_inv): the forward product of the row-quantized bf16
+    activations x [M][K] with the packed weights Wp [N][ceil(K/4)], the
+    quantizer fused into the product (see include/t3.h); C int32 [M][N]."""
+    torch = _torch()
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise TypeError("x must be a 2-D CUDA bfloat16 tensor [M][K]")
+    M, K = x.shape
+    N = Wp.shape[0]
+    if Wp.dim() != 2 or Wp.shape[1] != (K + 3) // 4:
+        raise ValueError("Wp must be [N][ceil(K/4)]")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.int32, device=x.device)
+    if row_scale is None:
+        row_scale = torch.empty((M,), dtype=torch.float32, device=x.device)
+    if row_inv is None:
+        row_inv = torch.empty((M,), dtype=torch.float32, device=x.device)
+    if tuple(C.shape) != (M, N) or tuple(row_scale.shape) != (M,) or tuple(row_inv.shape) != (M,):
+        raise ValueError("C must be [M][N], row_scale and row_inv [M]")
+    args = (_dev_ptr(x, torch.bfloat16, "x"), _dev_ptr(Wp, torch.uint8, "Wp"),
+            _dev_ptr(C, torch.int32, "C"), _dev_ptr(row_scale, torch.float32, "row_scale"),
+            _dev_ptr(row_inv, torch.float32, "row_inv"), M, N, K, _stream(x, stream))
+    with torch.cuda.device(x.device):
+        rc = load().t3_gemm_fwd_bf16(*args)
+    _check(rc, "t3_gemm_fwd_bf16")
+    return C, row_scale, row_inv
 
 
 def t3_dequant_i32(x, kind=T3_OUT_F32, row_scale=None, col_scale=None, out=None, stream=None):

@@ -68,6 +68,25 @@ bool make_i32_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_
   return r == CUDA_SUCCESS;
 }
 
+// bf16 matrix [rows][cols] (cols elements of 2 bytes per row) as 16-bit
+// elements, boxes of box_cols x box_rows in the 128-byte swizzle.
+bool make_u16_map_tiled(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                        int box_rows, int box_cols) {
+  std::memset(map, 0, sizeof(*map));
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (cols * 2) % 16 != 0) return false;
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) std::memset(map, 0, sizeof(*map));
+  return r == CUDA_SUCCESS;
+}
+
 // Output tensor map of the pair pipeline for output kind `kind` (tc2::kOutI32
 // or a T3_OUT_* kind): boxes of 32 columns x 128 rows; int32 and float rows
 // in the 128-byte swizzle, bf16 rows (64 bytes) unswizzled.
@@ -510,6 +529,67 @@ int t3_last_device_error(t3_stream_t stream, int32_t* detail) {
   if (detail) *detail = value;
   if (value == 0) return T3_OK;
   return (value & 0xFF) == 6 ? T3_EVALUE : T3_ETIMEOUT;  // role 6: an invalid input value
+}
+
+int t3_gemm_fwd_bf16(const void* X, const uint8_t* Wp, int32_t* C, float* row_scale,
+                     float* row_inv, int64_t M, int64_t N, int64_t K, t3_stream_t stream) {
+  if (bad_dims(M, N, K)) return T3_EINVAL;
+  if (M == 0) return T3_OK;
+  if (!row_scale || !row_inv || (K > 0 && !X)) return T3_EINVAL;
+  if (K > kMaxTernaryReduction) return T3_EOVERFLOW;
+  // the fused kernel's shapes, checked before any CUDA call
+  if (N > 0 && K > 0 &&
+      (M <= kSmallM || K % 64 != 0 || reinterpret_cast<uintptr_t>(X) % 16 != 0 ||
+       reinterpret_cast<uintptr_t>(Wp) % 16 != 0))
+    return T3_EINVAL;
+  const DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != T3_OK) return st;
+  if (K == 0) {  // zero rows: scales 0, and the empty reduction writes zeros
+    if (cudaMemsetAsync(row_scale, 0, M * sizeof(float), stream) != cudaSuccess ||
+        cudaMemsetAsync(row_inv, 0, M * sizeof(float), stream) != cudaSuccess)
+      return T3_ECUDA;
+    return N == 0 ? T3_OK : zero_fill(C, M, N, stream);
+  }
+  if (N > 0 && (!Wp || !C)) return T3_EINVAL;
+  // the fused kernel's shapes: checked before anything is launched
+  const int64_t KB = (K + 3) / 4;
+  CUtensorMap ma, mw, mo;
+  if (N > 0) {
+    if (!make_u16_map_tiled(&ma, X, M, K, 128, tc2::BK / 2)) return T3_EINVAL;
+    if (!make_u8_map_tiled(&mw, Wp, N, KB, KB, tc2::BNH, tc2::BK / 4)) return T3_EINVAL;
+    if (!make_out_map(&mo, C, M, N, tc2::kOutI32)) mo = mw;  // plain stores
+  }
+  st = launch_row_scales(X, row_scale, row_inv, M, K, dev->sms, stream);
+  if (st != T3_OK || N == 0) return st;
+  tc2::Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.out_rows = M;
+  p.out_cols = N;
+  p.num_stages = ceil_div(K, tc2::BK);
+  const int64_t tiles_r = ceil_div(M, tc2::BMP), tiles_c = ceil_div(N, tc2::BN);
+  if (tiles_r * tiles_c > kMaxDim) return T3_EINVAL;
+  p.tiles_r = static_cast<int>(tiles_r);
+  p.tiles_c = static_cast<int>(tiles_c);
+  p.out = C;
+  p.use_tma_out = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && (N * 4) % 16 == 0) ? 1 : 0;
+  p.out_kind = tc2::kOutI32;
+  p.wp = Wp;
+  p.kb_bytes = KB;
+  p.w_tma = 1;
+  p.w_vec4 = 1;
+  p.act = nullptr;
+  p.act_rows = M;
+  p.act_cols = K;
+  p.a_tma = 1;
+  p.mode = tc2::kModeBf16;
+  p.dp_tiles = static_cast<int>(tiles_r * tiles_c);
+  p.row_inv = row_inv;
+  p.err = dev->err_word;
+  const int64_t pairs = std::min<int64_t>(tiles_r * tiles_c, std::max(dev->sms / 2, 1));
+  return launch_tc2_fwd_bf16(p, ma, mw, mo, static_cast<int>(2 * pairs), stream);
 }
 
 int t3_selftest_wait_timeout(int64_t limit_ns, t3_stream_t stream) {

@@ -29,6 +29,11 @@ int launch_tc2_dx(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap
 int prepare_tc2_fwd();
 int prepare_tc2_dx();
 
+// The forward on bf16 activations quantized in the pair pipeline's converters
+// (tc2::kModeBf16; p.row_inv holds the rows' inverse scales).
+int launch_tc2_fwd_bf16(const tc2::Params& p, const CUtensorMap& ma, const CUtensorMap& mw,
+                        const CUtensorMap& mo, int grid, cudaStream_t s);
+
 // Zeroes out[0, n) on `s` as a programmatic dependent of the work before it:
 // it waits for that work to complete, then lets the next grid launch early.
 int launch_zero_pdl(int32_t* out, int64_t n, int sms, cudaStream_t s);
@@ -46,6 +51,11 @@ int launch_pack_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N, int s
 
 // bf16 x [M][K] -> int8 q [M][K] and a float scale per row (absmax), on `s`.
 int launch_quant_rows(const void* x, int8_t* q, float* scale, int64_t M, int64_t K, int sms,
+                      cudaStream_t s);
+
+// The row quantizer's scales only: scale = amax / 127 and inv = 127 / amax per
+// row of bf16 x [M][K] (0 and 0 for a zero row), on `s`.
+int launch_row_scales(const void* x, float* scale, float* inv, int64_t M, int64_t K, int sms,
                       cudaStream_t s);
 
 // out[r][c] = scaled int32 x[r][c] (T3_OUT_* kind), on `s`.

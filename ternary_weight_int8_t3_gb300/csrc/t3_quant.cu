@@ -37,9 +37,14 @@ __device__ __forceinline__ int8_t quant1(float x, float inv) {
   return static_cast<int8_t>(q);
 }
 
+// kCodes: write the int8 codes (else only the scales, and `inv`: the inverse
+// scales 127 / amax of the same division, for a product that quantizes the
+// rows itself).
+template <bool kCodes>
 __global__ void __launch_bounds__(32 * kWarps) quant_rows_kernel(const uint16_t* __restrict__ x,
                                                                  int8_t* __restrict__ q,
                                                                  float* __restrict__ scale,
+                                                                 float* __restrict__ inv_out,
                                                                  int64_t M, int64_t K, int vec) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * kWarps;
@@ -65,6 +70,10 @@ __global__ void __launch_bounds__(32 * kWarps) quant_rows_kernel(const uint16_t*
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
     if (lane == 0) scale[m] = amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 0.0f;
+    if (!kCodes) {
+      if (lane == 0) inv_out[m] = inv;
+      continue;
+    }
     if (vec) {
       for (int64_t k = 8 * lane; k < K; k += 256) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + k));
@@ -93,8 +102,19 @@ int launch_quant_rows(const void* x, int8_t* q, float* scale, int64_t M, int64_t
   const int64_t blocks = (M + qz::kWarps - 1) / qz::kWarps;
   const int64_t cap = 8 * static_cast<int64_t>(sms > 0 ? sms : 1);
   const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
-  qz::quant_rows_kernel<<<grid, 32 * qz::kWarps, 0, s>>>(static_cast<const uint16_t*>(x), q, scale,
-                                                        M, K, vec);
+  qz::quant_rows_kernel<true><<<grid, 32 * qz::kWarps, 0, s>>>(static_cast<const uint16_t*>(x), q,
+                                                              scale, nullptr, M, K, vec);
+  return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
+}
+
+int launch_row_scales(const void* x, float* scale, float* inv, int64_t M, int64_t K, int sms,
+                      cudaStream_t s) {
+  const int vec = (K % 8 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
+  const int64_t blocks = (M + qz::kWarps - 1) / qz::kWarps;
+  const int64_t cap = 8 * static_cast<int64_t>(sms > 0 ? sms : 1);
+  const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
+  qz::quant_rows_kernel<false><<<grid, 32 * qz::kWarps, 0, s>>>(static_cast<const uint16_t*>(x),
+                                                               nullptr, scale, inv, M, K, vec);
   return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
 }
 

@@ -66,9 +66,12 @@ template <int OP> struct RawW;
 template <> struct RawW<kOpFwd> { static constexpr int rows = BNH, cols = BK / 4; };  // [96 n][32 B]
 template <> struct RawW<kOpDx> { static constexpr int rows = BK, cols = BN / 4; };     // [128 n][48 B]
 
-template <int OP> struct Layout {
+// kActBytes: bytes per raw activation element (1 for int8; 2 for the bf16
+// activations the fused quantizer reads, as two 64-element boxes per stage)
+template <int OP, int kActBytes = 1> struct Layout {
+  static constexpr int raw_a = RAW_A * kActBytes;
   static constexpr int raw_w = RawW<OP>::rows * RawW<OP>::cols;
-  static constexpr int raw_stage = ((RAW_A + raw_w) + 1023) / 1024 * 1024;
+  static constexpr int raw_stage = ((raw_a + raw_w) + 1023) / 1024 * 1024;
   static constexpr int opb_atom = BNH * 128;          // forward: [96 rows][64 f16]
   // forward: two 64-element k atoms, K-major; dX: MN-major, per 8 n rows two
   // 64-element k atoms (the CTA's 96 k fill one and a half)
@@ -118,6 +121,8 @@ struct Params {
   // output rows that a chained grid has zeroed; when dp_tiles < tiles_r *
   // tiles_c every output write waits for that grid.
   int dp_tiles;
+  // kModeBf16: the inverse row scales 127 / amax of the bf16 activations
+  const float* row_inv;
   int* err;
 };
 
@@ -172,6 +177,9 @@ __device__ __forceinline__ int chunk_end(int c0, int kb1) {
 // whole words (activations by TMA); and the general one, where each operand
 // comes by TMA or from global memory as p.a_tma / p.w_tma say.
 constexpr int kModeTma = 0, kModeWGlobal = 1, kModeAGlobal = 2;
+// The forward with bf16 activations quantized in the converters (both
+// operands by TMA, whole tiles, int32 output).
+constexpr int kModeBf16 = 3;
 
 // Scaled epilogue: y = ((float)x * rs) * cs per element, each product rounded
 // to nearest (no contraction); x is the accumulator, an exact integer in f32
@@ -566,6 +574,59 @@ __device__ __forceinline__ void w_dx_store(uint8_t* opb, int tid, const uint32_t
   }
 }
 
+// Two bf16 activations (the high halves of fa and fb, low halves zero) ->
+// their int8 codes of the row quantizer, q = rint(fl(x * inv)), as an exact
+// f16 pair (q(a) low, q(b) high).  Adding 1.5 * 2^23 + 128 rounds a product
+// p, |p| <= 127.00002 (|x| <= amax, inv = fl(127 / amax)), to the nearest
+// integer with ties to even, and leaves q + 128 in the low 10 bits of the sum;
+// f16 0x6400 | (q + 128) is 1024 + q + 128, and subtracting 1152 leaves q.
+// No clamp is needed: |rint(p)| <= 127.
+__device__ __forceinline__ uint32_t quant_pair_f16(uint32_t fa, uint32_t fb, float inv) {
+  const float ta = __fadd_rn(__fmul_rn(__uint_as_float(fa), inv), 12583040.0f);
+  const float tb = __fadd_rn(__fmul_rn(__uint_as_float(fb), inv), 12583040.0f);
+  const uint32_t packed = (__float_as_uint(ta) & 0x3FFu) | ((__float_as_uint(tb) & 0x3FFu) << 16);
+  return hsub2(packed | 0x64006400u, 0x64806480u);
+}
+
+// The same for a row whose inverse scale is infinite (amax so small that
+// 127 / amax overflows): x * inf is +-inf, clamped to +-127, and 0 * inf counts
+// as 0.
+__device__ __forceinline__ uint32_t quant_pair_f16_inf(uint32_t fa, uint32_t fb) {
+  const float a = __uint_as_float(fa), b = __uint_as_float(fb);
+  const uint32_t ua = a > 0.0f ? 255u : (a < 0.0f ? 1u : 128u);
+  const uint32_t ub = b > 0.0f ? 255u : (b < 0.0f ? 1u : 128u);
+  return hsub2((ua | (ub << 16)) | 0x64006400u, 0x64806480u);
+}
+
+// bf16 activation row -> quantized f16 pairs for TMEM: thread (quadrant q,
+// half h) owns row `row` and reduction elements [64h, 64h+64) of the stage,
+// which are box h of the raw stage ([128 rows][128 B] in the 128-byte
+// swizzle).  Same order as act_load<true>: within every 16 elements the even
+// ones first, then the odd ones.
+__device__ __forceinline__ void act_load_bf16(const uint8_t* raw_a, int row, int h, float inv,
+                                              bool inv_finite, uint32_t (&v)[32]) {
+  const uint8_t* box = raw_a + h * RAW_A;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    // 16 elements: words w[2j], w[2j+1] hold elements (4j, 4j+1), (4j+2, 4j+3)
+    const uint4 x0 = *reinterpret_cast<const uint4*>(box + tc::sw128(row, 2 * c));
+    const uint4 x1 = *reinterpret_cast<const uint4*>(box + tc::sw128(row, 2 * c + 1));
+    const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t ea = w[2 * j] << 16, eb = w[2 * j + 1] << 16;                 // 4j, 4j+2
+      const uint32_t oa = w[2 * j] & 0xFFFF0000u, ob = w[2 * j + 1] & 0xFFFF0000u;  // 4j+1, 4j+3
+      if (inv_finite) {
+        v[8 * c + j] = quant_pair_f16(ea, eb, inv);
+        v[8 * c + 4 + j] = quant_pair_f16(oa, ob, inv);
+      } else {
+        v[8 * c + j] = quant_pair_f16_inf(ea, eb);
+        v[8 * c + 4 + j] = quant_pair_f16_inf(oa, ob);
+      }
+    }
+  }
+}
+
 // How many stages one pair runs in all (whole tiles and stream-K pieces).
 __device__ __forceinline__ int64_t pair_stage_count(const Params& p, int pair, int npairs) {
   const int64_t whole = pair < p.dp_tiles ? (p.dp_tiles - 1 - pair) / npairs + 1 : 0;
@@ -583,7 +644,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap map_w,
                const __grid_constant__ CUtensorMap map_out) {
   static_assert(!kSplit || kMode == kModeTma, "the split schedule takes TMA operands");
-  using L = Layout<OP>;
+  static_assert(kMode != kModeBf16 || (OP == kOpFwd && !kSplit), "bf16 activations: forward, whole tiles");
+  using L = Layout<OP, kMode == kModeBf16 ? 2 : 1>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((base_addr + 1023u) & ~1023u) - base_addr);
@@ -615,7 +677,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // without weight TMA only the activation warps read the raw stages
       // the warps that read the raw stages release them
       const int readers = (p.a_tma ? kActWarps : 0) + (p.w_tma ? kWWarps : 0);
-      mbar_init(&raw_empty[s], kMode == kModeTma ? kConvWarps
+      mbar_init(&raw_empty[s], (kMode == kModeTma || kMode == kModeBf16) ? kConvWarps
                                : kMode == kModeWGlobal ? kActWarps
                                : (readers > 0 ? readers : 1));
     }
@@ -666,6 +728,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // the split schedule only needs the count of the pair's stages here
     int64_t left = kSplit ? pair_stage_count(p, pair, npairs) : 0;
     for (int tile = pair; ok && tile < (kSplit ? pair + 1 : num_tiles); tile += npairs) {
+      // bf16 activations: this thread's row's inverse scale
+      float row_inv = 0.0f;
+      bool inv_finite = true;
+      if constexpr (kMode == kModeBf16) {
+        const int64_t m = static_cast<int64_t>(tile / p.tiles_c) * BMP + rank * 128 + row;
+        row_inv = (act_warp && m < p.M) ? __ldg(p.row_inv + m) : 0.0f;
+        inv_finite = row_inv <= 3.402823466e38f;  // false for +inf
+      }
       for (int64_t kb = 0; kSplit ? left-- > 0 : kb < p.num_stages; ++kb) {
         const uint8_t* ra = raw + rs * L::raw_stage;
         const uint32_t act_taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kActCol +
@@ -719,12 +789,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         uint32_t v[32];
-        if (act_warp)
-          act_load<OP == kOpFwd>(ra, row, h, v);
-        else if (OP == kOpFwd)
-          w_fwd_load(ra + RAW_A, wtid, v);
-        else
-          w_dx_load(ra + RAW_A, wtid, rank, v);
+        if (act_warp) {
+          if constexpr (kMode == kModeBf16)
+            act_load_bf16(ra, row, h, row_inv, inv_finite, v);
+          else
+            act_load<OP == kOpFwd>(ra, row, h, v);
+        } else if (OP == kOpFwd) {
+          w_fwd_load(ra + L::raw_a, wtid, v);
+        } else {
+          w_dx_load(ra + L::raw_a, wtid, rank, v);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[rs]);
         ok = mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
@@ -786,13 +860,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (lane == 0) {
           uint8_t* dst = raw + stage * L::raw_stage;
-          mbar_arrive_expect_tx(&raw_full[stage], (ag_p ? 0 : RAW_A) + (wg_p ? 0 : L::raw_w));
-          if (!ag_p) tma_load_2d(dst, &map_a, &raw_full[stage], static_cast<int>(kb * BK), ay);
+          mbar_arrive_expect_tx(&raw_full[stage], (ag_p ? 0 : L::raw_a) + (wg_p ? 0 : L::raw_w));
+          if (kMode == kModeBf16) {
+            // two boxes of 64 bf16 (128 B) x 128 rows
+            tma_load_2d(dst, &map_a, &raw_full[stage], static_cast<int>(kb * BK), ay);
+            tma_load_2d(dst + RAW_A, &map_a, &raw_full[stage], static_cast<int>(kb * BK + BK / 2), ay);
+          } else if (!ag_p) {
+            tma_load_2d(dst, &map_a, &raw_full[stage], static_cast<int>(kb * BK), ay);
+          }
           if (!wg_p) {
             if (OP == kOpFwd)
-              tma_load_2d(dst + RAW_A, &map_w, &raw_full[stage], static_cast<int>(kb * (BK / 4)), wy);
+              tma_load_2d(dst + L::raw_a, &map_w, &raw_full[stage], static_cast<int>(kb * (BK / 4)), wy);
             else
-              tma_load_2d(dst + RAW_A, &map_w, &raw_full[stage], wx, static_cast<int>(kb * BK));
+              tma_load_2d(dst + L::raw_a, &map_w, &raw_full[stage], wx, static_cast<int>(kb * BK));
           }
         }
         issued_mask |= 1u << stage;

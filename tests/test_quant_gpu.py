@@ -98,3 +98,86 @@ def test_quantize_then_scaled_forward():
     qo, so = oracle.quantize_rows(bits)
     want = oracle.dequant(oracle.fwd(qo, wp), so, None)
     np.testing.assert_array_equal(C.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
+# ------------------------------------------------------- the fused forward --
+# t3_gemm_fwd_bf16: the row quantizer inside the forward product (the bf16
+# tiles are quantized by the pair pipeline's converters).  Its result must be
+# that of the chain it replaces, oracle.quantize_rows then oracle.fwd, bit for
+# bit, and its scales those of the quantizer.
+
+def _fused(bits, wp, offset=0):
+    M, K = bits.shape
+    buf = torch.zeros(M * K + offset + 8, dtype=torch.int16, device="cuda")
+    x = buf[offset:offset + M * K].view(M, K).view(torch.bfloat16)
+    x.view(torch.int16).copy_(torch.from_numpy(bits.view(np.int16)))
+    C, s, inv = t3.t3_gemm_fwd_bf16(x, torch.from_numpy(wp).cuda())
+    torch.cuda.synchronize()
+    return C.cpu().numpy(), s.cpu().numpy(), inv.cpu().numpy()
+
+
+def _inv_want(bits):
+    x = (bits.astype(np.uint32) << 16).view(np.float32)
+    amax = np.abs(x).max(axis=1)
+    with np.errstate(divide="ignore", over="ignore"):
+        return np.where(amax > 0, np.float32(127) / amax, np.float32(0)).astype(np.float32)
+
+
+@pytest.mark.parametrize("M,N,K", [(33, 272, 64), (300, 200, 1280), (257, 201, 192),
+                                   (1000, 384, 4096)])
+def test_fused_forward_matches_quantize_then_forward(M, N, K):
+    g = t3_synth.rng(M * 3 + N + K)
+    bits = _rows(g, M, K)
+    bits[1] = 0                                    # a zero row: scale 0, codes 0
+    bits[2] = _bf16_bits(np.full(K, 1e-37, np.float32) * np.sign(g.standard_normal(K)))
+    bits[2, :5] = 0                                # 127 / amax overflows: codes +-127 and 0
+    wp = oracle.pack(t3_synth.ternary(g, (K, N)))
+    C, s, inv = _fused(bits, wp)
+    q, s_want = oracle.quantize_rows(bits)
+    np.testing.assert_array_equal(s.view(np.uint32), s_want.view(np.uint32))
+    np.testing.assert_array_equal(inv.view(np.uint32), _inv_want(bits).view(np.uint32))
+    np.testing.assert_array_equal(C, oracle.fwd(q, wp))
+
+
+def test_fused_forward_ties_and_the_library_chain():
+    """Rows whose products fall on .5 (ties to even) and the library's own
+    unfused chain (t3_quantize_rows_bf16, then t3_gemm_fwd) giving the same C."""
+    M, N, K = 96, 192, 128
+    g = t3_synth.rng(55)
+    vals = np.array([127.0, 0.5, 1.5, 2.5, -0.5, -2.5, 63.5, -63.5], np.float32)
+    bits = _bf16_bits(g.choice(vals, size=(M, K)))
+    bits[:, 0] = _bf16_bits(np.full(M, 127.0, np.float32))   # amax 127: inv = 1
+    wp = oracle.pack(t3_synth.ternary(g, (K, N)))
+    C, s, _ = _fused(bits, wp)
+    q, s_want = oracle.quantize_rows(bits)
+    np.testing.assert_array_equal(C, oracle.fwd(q, wp))
+    x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    q_lib, _ = t3.t3_quantize_rows_bf16(x)
+    C_lib = t3.t3_gemm_fwd(q_lib, torch.from_numpy(wp).cuda(), K=K)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(C, C_lib.cpu().numpy())
+
+
+def test_fused_forward_layer_shape():
+    M, N, K = 16384, 3456, 1280
+    g = t3_synth.rng(16384)
+    bits = _bf16_bits((g.standard_normal((M, K)) * 3).astype(np.float32))
+    wp = oracle.pack(t3_synth.ternary(g, (K, N)))
+    C, s, _ = _fused(bits, wp)
+    q, s_want = oracle.quantize_rows(bits)
+    np.testing.assert_array_equal(s.view(np.uint32), s_want.view(np.uint32))
+    np.testing.assert_array_equal(C, oracle.fwd(q, wp))
+
+
+def test_fused_forward_rejects_shapes_it_does_not_take():
+    lib = t3.load()
+    f = lib.t3_gemm_fwd_bf16
+    x = torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda")
+    wp = torch.zeros((16, 32), dtype=torch.uint8, device="cuda")
+    C = torch.empty((64, 16), dtype=torch.int32, device="cuda")
+    sc = torch.empty(64, dtype=torch.float32, device="cuda")
+    inv = torch.empty(64, dtype=torch.float32, device="cuda")
+    P = lambda t: t.data_ptr()
+    assert f(P(x), P(wp), P(C), P(sc), P(inv), 32, 16, 128, None) == t3.T3_EINVAL   # M <= 32
+    assert f(P(x), P(wp), P(C), P(sc), P(inv), 64, 16, 96, None) == t3.T3_EINVAL    # K % 64
+    assert f(P(x) + 2, P(wp), P(C), P(sc), P(inv), 63, 16, 128, None) == t3.T3_EINVAL  # X unaligned
