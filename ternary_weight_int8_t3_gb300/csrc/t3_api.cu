@@ -123,6 +123,8 @@ constexpr int64_t kMaxInt8Reduction = 131071;       // 16384 * M <= INT32_MAX
 // zeroing grid and the dependent launch before it cost nothing measurable.
 constexpr int64_t kSplitCostStages = 8;
 constexpr int64_t kSmallM = 32;                     // forward rows served by the small-M path
+constexpr int64_t kGemvM = 8;                       // of those, at most the rows the CUDA cores serve
+constexpr int64_t kGemvSmallBytes = 4 << 20;        // packed weights up to which they serve 3..8 rows
 
 struct DeviceInfo {
   bool ready = false;
@@ -388,6 +390,13 @@ int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64
     const DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st != T3_OK) return st;
+    // the CUDA-core path: one or two rows, or up to eight over few weights
+    // (measured: it beats the tensor cores there; the tensor cores win from
+    // four rows at N = K = 8192)
+    if (M <= 2 || (M <= kGemvM && N * ((K + 3) / 4) <= kGemvSmallBytes)) {
+      st = launch_gemv_fwd(A, Wp, C, M, N, K, dev->sms, stream);
+      if (st != T3_EINVAL) return st;
+    }
     return launch_skinny_fwd(A, Wp, C, M, N, K, dev->sms, dev->err_word, stream);
   }
   return run_tc2<kOpFwd>(A, Wp, C, M, N, K, stream);

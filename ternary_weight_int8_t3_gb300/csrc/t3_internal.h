@@ -62,7 +62,12 @@ int launch_row_scales(const void* x, float* scale, float* inv, int64_t M, int64_
 int launch_dequant(const int32_t* x, void* out, int64_t rows, int64_t cols, const float* row_scale,
                    const float* col_scale, int kind, int sms, cudaStream_t s);
 
-// Small-M forward (M <= 32): zeroes C on `s`, then accumulates into it.
+// Forward for M <= 8 on the CUDA cores (t3_gemv.cu); T3_EINVAL, with nothing
+// launched, when A's copy would not fit its shared-memory budget.
+int launch_gemv_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,
+                    int64_t K, int sms, cudaStream_t s);
+
+// Small-M forward (M <= 32) on the tensor cores.
 int launch_skinny_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,
                       int64_t K, int sms, int* err, cudaStream_t s);
 
