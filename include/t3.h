@@ -97,7 +97,9 @@ int t3_pack_ternary_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N,
  *   A [M][K], Wp [N][ceil(K/4)], C [M][N] (layouts above), device pointers.
  * Exact for every input when K <= 16777215 (|A W| <= 128 K fits int32);
  * larger K returns T3_EOVERFLOW.  M <= 32 takes the small-M path, which is
- * bound by reading the packed weights: it enqueues one kernel on `stream` as
+ * bound by reading the packed weights: one or two rows (and up to eight when
+ * Wp is at most 4 MB) run on the CUDA cores (byte-permute decode, dp4a), the
+ * rest on the tensor cores.  Either way it enqueues one kernel on `stream` as
  * a programmatic dependent of the work before it, so that its launch and set-
  * up overlap that work's end; it reads A and Wp and writes C only after all
  * earlier work on `stream` has completed.

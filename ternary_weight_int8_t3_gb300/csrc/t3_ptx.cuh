@@ -70,9 +70,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits until the phase with the given parity has completed.  Bounded: on
-// timeout (or when another role of the CTA has aborted) it records `code` in
-// *err (first writer wins), raises *abort_flag and returns false.
 // As mbar_try_wait, but the thread may stay suspended up to `hint_ns` waiting
 // for the phase instead of returning at once (fewer shared-memory polls).
 __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
@@ -108,6 +105,9 @@ __device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Waits until the phase with the given parity has completed.  Bounded: on
+// timeout (or when another role of the CTA has aborted) it records `code` in
+// *err (first writer wins), raises *abort_flag and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag, int* err, int code) {
   return mbar_wait_limit(bar, parity, abort_flag, err, code, kWaitLimitNs);
@@ -196,8 +196,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy reads (the tensor core reading operands).
 // Waits until the grids this one depends on programmatically have completed
 // and their writes are visible; a no-op without such a dependency.
 __device__ __forceinline__ void grid_dependency_wait() {
@@ -209,6 +207,8 @@ __device__ __forceinline__ void launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads (the tensor core reading operands).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
