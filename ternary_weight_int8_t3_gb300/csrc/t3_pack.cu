@@ -21,13 +21,13 @@
 // store.
 //
 // Where w can be a TMA source (rows of a multiple of 16 bytes, 16-byte aligned
-// base), one CTA per SM walks the tiles with the loads decoupled from the
-// packing: a producer warp streams them by TMA into a ring of eight stages
-// (~128 KB per SM in flight), and three groups of eight warps pack the tiles
-// in turn with the same per-thread work as above.  Tiles past K or N arrive
-// zero-filled (code 0, as the pad positions want).  (Tiles of two stages, so
-// that each column's packed bytes fill a 32-byte sector of Wp, measured no
-// faster.)
+// base), one CTA per SM walks tiles of 128 k x 128 n with the loads decoupled
+// from the packing: a producer warp streams them by TMA into a ring of nine
+// stages (~144 KB per SM in flight), and three groups of eight warps pack the
+// tiles in turn, each group on its own three stages, with the same per-thread
+// work as above.  A column's 32 packed bytes of a tile fill one sector of its
+// Wp row, written by two neighbouring lanes.  Tiles past K or N arrive
+// zero-filled (code 0, as the pad positions want).
 #include <atomic>
 #include <cstdint>
 
@@ -74,17 +74,39 @@ __device__ __forceinline__ uint32_t codes4(uint32_t x, bool& bad) {
 // four k (codes fill 2 bits, so nothing crosses into the next byte).  A 4 x 4
 // byte transpose of the four such words gives out[i], column i's 4 packed
 // bytes (16 k).
-__device__ __forceinline__ void pack_tile(const int8_t (*tile)[TN], int cg, int kq,
+template <int kRow>
+__device__ __forceinline__ void pack_tile(const int8_t (*tile)[kRow], int cg, int kq,
                                           uint32_t (&out)[4], bool& bad) {
   uint32_t q[4];
+  // per byte lo = bit 0 and sg = the sign bit of every word; the code words
+  // of four rows (lo + sg in bits 2 rr of each byte) add up as lo0 + sg0 +
+  // 4 (lo1 + sg1) + 16 (..) + 64 (..), the fields never overlapping, so the
+  // merge is multiply-adds; one validity word collects every byte that lo |
+  // (sg * 0xFF) does not rebuild, and only a tile part with such a byte
+  // takes the byte-by-byte path (invalid values as code 0)
+  uint32_t x[16], any_bad = 0u;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] = *reinterpret_cast<const uint32_t*>(&tile[16 * kq + i][4 * cg]);
 #pragma unroll
   for (int sb = 0; sb < 4; ++sb) {
-    const int r = 16 * kq + 4 * sb;
     uint32_t word = 0u;
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr)
-      word |= codes4(*reinterpret_cast<const uint32_t*>(&tile[r + rr][4 * cg]), bad) << (2 * rr);
+    for (int rr = 0; rr < 4; ++rr) {
+      const uint32_t xv = x[4 * sb + rr];
+      const uint32_t lo = xv & 0x01010101u, sg = (xv >> 7) & 0x01010101u;
+      any_bad |= (lo | (sg * 0xFFu)) ^ xv;
+      word += (lo + sg) * (1u << (2 * rr));
+    }
     q[sb] = word;
+  }
+  if (any_bad != 0u) {
+#pragma unroll
+    for (int sb = 0; sb < 4; ++sb) {
+      uint32_t word = 0u;
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) word |= codes4(x[4 * sb + rr], bad) << (2 * rr);
+      q[sb] = word;
+    }
   }
   const uint32_t a = byte_perm(q[0], q[1], 0x5140u), b = byte_perm(q[2], q[3], 0x5140u);
   const uint32_t c = byte_perm(q[0], q[1], 0x7362u), d = byte_perm(q[2], q[3], 0x7362u);
@@ -132,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const int8_t* __restrict
     __syncthreads();
     // rows past K hold 0 and pack as code 0
     uint32_t out[4];  // per column: 4 packed bytes = 16 k
-    pack_tile(tile, cg, kq, out, bad);
+    pack_tile<TN>(tile, cg, kq, out, bad);
 #pragma unroll
     for (int i = 0; i < 4; ++i) packed[4 * cg + i][kq] = out[i];
     __syncthreads();
@@ -155,27 +177,34 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const int8_t* __restrict
   if (__any_sync(0xffffffffu, bad) && (t & 31) == 0) atomicCAS(err, 0, kErrInvalid);
 }
 
-constexpr int kStages = 8;
 constexpr int kGroups = 3;                          // consumer groups, tiles in turn
-constexpr int kSub = 1;                             // 64-row ring stages per tile
+// Tile i goes to stage i % kStages and to group i % kGroups; with kStages a
+// multiple of kGroups every stage belongs to one group, which consumes its
+// stages in order.  A group can then never wait on a stage whose previous
+// tile (another group's) has not landed yet, where the parity wait would
+// match the completion two phases back and pass early.
+constexpr int kStages = 3 * kGroups;
 constexpr int kTmaThreads = kGroups * kThreads + 32;  // + the producer warp
-constexpr int kTileBytes = TK * TN;
+// the TMA path's tiles: 128 k x 128 n (16 KB), so that a column's packed
+// bytes of a tile (32) fill a sector of its Wp row, written by two lanes
+constexpr int TK2 = 128, TN2 = 128;
+constexpr int kTileBytes = TK2 * TN2;
 constexpr int kTmaSmem = kStages * kTileBytes + 128;
-constexpr int kRowWords = 4 * kSub;                 // packed words per column per tile
-static_assert(kGroups * kSub <= kStages, "every group can hold its tile's stages");
+constexpr int kRowWords = TK2 / 16;                 // packed words per column per tile
+static_assert(kStages % kGroups == 0, "each stage belongs to one consumer group");
+static_assert((TN2 / 4) * (TK2 / 16) == kThreads, "a thread packs 4 columns x 16 k");
 
-// Tiles of kSub * 64 k x 256 n, numbered n-block fastest; each column of a
-// tile makes kSub * 16 packed bytes of its Wp row.
+// Tiles of 128 k x 128 n, numbered n-block fastest; each column of a tile
+// makes 32 packed bytes of its Wp row.
 __global__ void __launch_bounds__(kTmaThreads, 1)
     pack_tma_kernel(const __grid_constant__ CUtensorMap map_w, uint8_t* __restrict__ wp,
                     int64_t N, int64_t KB, int64_t tiles_n, int64_t tiles, int vec_out,
                     int* err) {
   extern __shared__ uint8_t smem_raw[];
-  int8_t (*ring)[TK][TN] = reinterpret_cast<int8_t (*)[TK][TN]>(
+  int8_t (*ring)[TK2][TN2] = reinterpret_cast<int8_t (*)[TK2][TN2]>(
       smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u));
-  // a group's packed rows, padded by one word so that the 4-byte stores of
-  // consecutive column groups spread over the banks
-  __shared__ uint32_t packed[kGroups][TN][kRowWords + 1];
+  // a group's packed rows (two buffers), padded by one word
+  __shared__ uint32_t packed[kGroups][2][TN2][kRowWords + 1];
   __shared__ uint64_t full[kStages], empty[kStages];
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -194,64 +223,65 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&map_w);
-      for (int64_t j = 0; j < my_tiles * kSub; ++j) {  // ring stage j: part j % kSub of a tile
+      int64_t j = 0;
+      for (; j < my_tiles; ++j) {
         const int s = static_cast<int>(j % kStages);
         if (!mbar_wait(&empty[s], static_cast<uint32_t>((j / kStages) & 1) ^ 1u, &abort_flag, err,
                        code))
           break;
-        const int64_t tix = blockIdx.x + (j / kSub) * gridDim.x;
+        const int64_t tix = blockIdx.x + j * gridDim.x;
         const int64_t tk = tix / tiles_n;
         mbar_arrive_expect_tx(&full[s], kTileBytes);
-        tma_load_2d(ring[s], &map_w, &full[s], static_cast<int32_t>((tix - tk * tiles_n) * TN),
-                    static_cast<int32_t>(tk * TK * kSub + (j % kSub) * TK));
+        tma_load_2d(ring[s], &map_w, &full[s], static_cast<int32_t>((tix - tk * tiles_n) * TN2),
+                    static_cast<int32_t>(tk * TK2));
       }
+      // no copy is left in flight when the CTA ends, whatever the consumers
+      // did (a wait of its own, bounded, that an abort does not cut short)
+      int keep_waiting = 0;
+      for (int64_t q = j - kStages < 0 ? 0 : j - kStages; q < j; ++q)
+        mbar_wait(&full[q % kStages], static_cast<uint32_t>((q / kStages) & 1), &keep_waiting, err,
+                  code);
     }
     return;
   }
   // ------------------------------------------------------------- consumers
   const int grp = warp / (kThreads / 32);
   const int t = threadIdx.x - grp * kThreads;
-  const int cg = t % (TN / 4), kq = t / (TN / 4);
+  const int cg = t % (TN2 / 4), kq = t / (TN2 / 4);
   bool bad = false;
   for (int64_t i = grp; i < my_tiles; i += kGroups) {
-    uint32_t out[kSub][4];
-    bool ok = true;
-#pragma unroll
-    for (int h = 0; h < kSub; ++h) {
-      const int64_t j = i * kSub + h;
-      const int s = static_cast<int>(j % kStages);
-      ok = mbar_wait(&full[s], static_cast<uint32_t>((j / kStages) & 1), &abort_flag, err,
-                     code + 1);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      pack_tile(ring[s], cg, kq, out[h], bad);
+    uint32_t out[4] = {0u, 0u, 0u, 0u};
+    const int s = static_cast<int>(i % kStages);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>((i / kStages) & 1),
+                                                     &abort_flag, err, code + 1));
+    if (ok) {
+      pack_tile<TN2>(ring[s], cg, kq, out, bad);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    if (!__all_sync(0xffffffffu, ok)) break;
     const int64_t tix = blockIdx.x + i * gridDim.x;
     const int64_t tk = tix / tiles_n;
-    const int64_t n0 = (tix - tk * tiles_n) * TN;
-    named_bar_sync(1 + grp, kThreads);  // this group's previous packed rows are stored
+    const int64_t n0 = (tix - tk * tiles_n) * TN2;
+    // two staging buffers per group, so that one barrier per tile separates
+    // this tile's stores from its reads, and the reads of the tile before
+    // (the other buffer) from the stores of the tile after; the barrier also
+    // takes the group's decision to stop (a wait that gave up), so that all
+    // its warps leave together and none is left at a later barrier
+    uint32_t (*pk)[kRowWords + 1] = packed[grp][(i / kGroups) & 1];
 #pragma unroll
-    for (int h = 0; h < kSub; ++h)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) packed[grp][4 * cg + c][4 * h + kq] = out[h][c];
-    named_bar_sync(1 + grp, kThreads);
-    const int64_t n = n0 + t;
-    const int64_t b0 = tk * (kSub * TK / 4);
-    if (n < N) {
-      uint8_t* dst = wp + n * KB + b0;
-      const uint32_t* row = packed[grp][t];
-#pragma unroll
-      for (int h = 0; h < kSub; ++h) {
-        const int64_t off = b0 + 16 * h;
-        if (vec_out && off + 16 <= KB) {
-          *reinterpret_cast<uint4*>(dst + 16 * h) =
-              make_uint4(row[4 * h], row[4 * h + 1], row[4 * h + 2], row[4 * h + 3]);
-        } else {
-          for (int b = 0; b < 16 && off + b < KB; ++b)
-            dst[16 * h + b] = static_cast<uint8_t>(row[4 * h + (b >> 2)] >> (8 * (b & 3)));
-        }
+    for (int c = 0; c < 4; ++c) pk[4 * cg + c][kq] = out[c];
+    if (!named_bar_and(1 + grp, kThreads, ok)) break;
+    // lanes 2 c and 2 c + 1: the two 16-byte halves of column c's 32 bytes
+    const int64_t n = n0 + (t >> 1);
+    const int hh = t & 1;
+    const int64_t off = tk * (TK2 / 4) + 16 * hh;
+    if (t < 2 * TN2 && n < N) {
+      uint8_t* dst = wp + n * KB + off;
+      const uint32_t* row = pk[t >> 1] + 4 * hh;
+      if (vec_out && off + 16 <= KB) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(row[0], row[1], row[2], row[3]);
+      } else {
+        for (int b = 0; b < 16 && off + b < KB; ++b) dst[b] = static_cast<uint8_t>(row[b >> 2] >> (8 * (b & 3)));
       }
     }
   }
@@ -268,7 +298,7 @@ int launch_pack_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N, int s
   const int vec_in = (N % 16 == 0) && (reinterpret_cast<uintptr_t>(w) % 16 == 0);
   const int vec_out = (KB % 16 == 0) && (reinterpret_cast<uintptr_t>(wp) % 16 == 0);
   CUtensorMap map;
-  if (vec_in && make_u8_map_tiled(&map, w, K, N, N, pack::TK, pack::TN, false)) {
+  if (vec_in && make_u8_map_tiled(&map, w, K, N, N, pack::TK2, pack::TN2, false)) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return T3_ECUDA;
     static std::atomic<bool> attr_done[64];
@@ -279,11 +309,11 @@ int launch_pack_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N, int s
         return T3_ECUDA;
       attr_done[dev].store(true, std::memory_order_release);
     }
-    const int64_t tiles_k2 = (K + pack::kSub * pack::TK - 1) / (pack::kSub * pack::TK);
-    const int64_t tiles2 = tiles_n * tiles_k2;
+    const int64_t tiles_n2 = (N + pack::TN2 - 1) / pack::TN2, tiles_k2 = (K + pack::TK2 - 1) / pack::TK2;
+    const int64_t tiles2 = tiles_n2 * tiles_k2;
     const int64_t grid = tiles2 < sms ? tiles2 : sms;
     pack::pack_tma_kernel<<<static_cast<unsigned>(grid > 0 ? grid : 1), pack::kTmaThreads,
-                            pack::kTmaSmem, s>>>(map, wp, N, KB, tiles_n, tiles2, vec_out, err);
+                            pack::kTmaSmem, s>>>(map, wp, N, KB, tiles_n2, tiles2, vec_out, err);
     return cudaGetLastError() == cudaSuccess ? T3_OK : T3_ECUDA;
   }
   // enough CTAs to keep every SM's loads in flight, each walking several tiles

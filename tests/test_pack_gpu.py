@@ -50,10 +50,11 @@ def _device_pack(w, w_offset=0, wp_offset=0):
 
 
 # rows of w that are a multiple of 16 bytes take the TMA-fed kernel (tiles of
-# 64 k x 256 n, zero-filled past K and N), the others the plain-load one
+# 128 k x 128 n, zero-filled past K and N), the others the plain-load one
+# (tiles of 64 k x 256 n)
 SHAPES = [(1, 1), (3, 5), (4, 16), (5, 7), (63, 127), (64, 128), (65, 129), (96, 272),
           (1000, 333), (130, 4096), (1280, 3456), (13, 64), (257, 1024), (8191, 16),
-          (4100, 2048)]
+          (4100, 2048), (192, 112), (640, 400), (127, 144), (129, 256)]
 
 
 @pytest.mark.parametrize("K,N", SHAPES)
