@@ -400,13 +400,24 @@ def bench_fused_quant(t3, torch, dev, stream, wp_d, reps=10):
     return out
 
 
-def bench_configs(t3, torch, dev, stream, peak, reps=20):
+# The pages' own forward timings of the shapes in their throughput table, in
+# ms per call on an RTX 4090 (launch overhead included): "t27c PTX backend:
+# ternary x int8 GEMM kernel emitted by a .t27 spec", section "Measured: RTX
+# 4090".  Context for the same shapes timed here, not a target.
+PAGES_FWD_MS = {(4096, 3456, 1280): 0.2211, (4096, 1280, 3456): 0.2538,
+                (4096, 1280, 1280): 0.0997, (16384, 3456, 1280): 0.8487,
+                (16384, 1280, 3456): 0.8345, (16384, 1280, 1280): 0.3359}
+
+
+def bench_configs(t3, torch, dev, stream, peak, reps=20,
+                  names=("fwd_square_4096", "bwd_1782x3456x1280")):
     """The other full-size workloads, each product timed on its own: the
     square forward 4096^3 (weights P(0) = 1/2) and the backward of the pages'
-    1782-row layer (dX over N = 3456, dW over the 1782 rows).  Enough sets of
-    buffers rotate through the calls that none is still in the 129 MB L2."""
+    1782-row layer (dX over N = 3456, dW over the 1782 rows), or the workloads
+    named.  Enough sets of buffers rotate through the calls that none is still
+    in the 129 MB L2."""
     out = {}
-    for name in ("fwd_square_4096", "bwd_1782x3456x1280"):
+    for name in names:
         wl = t3_synth.BY_NAME[name]
         A, w, dY = t3_synth.make_inputs(wl)
         wp = t3.t3_pack_ternary(w)
@@ -736,6 +747,16 @@ def main():
         line["quantized_fwd_bf16"] = bench_fused_quant(t3, torch, dev, stream, wp_d)
     if not args.step_only:
         line["configs"] = bench_configs(t3, torch, dev, stream, peak)
+        pages = bench_configs(t3, torch, dev, stream, peak,
+                              names=[f"fwd_{m}x{n}x{k}" for (m, n, k) in t3_synth.PAGES_FWD_SHAPES])
+        pages[f"fwd {M}x{N}x{K}"] = {"us": round(avg["fwd"] * 1e3, 2),
+                                     "TOPS": round(op_tops["fwd"], 1),
+                                     "frac": round(op_tops["fwd"] / peak, 3),
+                                     "timing": "the layer step's forward"}
+        for key, v in pages.items():
+            shape = tuple(int(x) for x in key.split()[1].split("x"))
+            v["pages_rtx4090_us"] = round(PAGES_FWD_MS[shape] * 1e3, 1)
+        line["pages_fwd_shapes"] = pages
     if not (args.no_pack or args.step_only):
         line["device_pack"] = {"hbm_peak_GBps": hbm, "calls": bench_device_pack(t3, torch, dev, stream, hbm)}
     if not (args.no_small_m or args.step_only):

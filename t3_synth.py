@@ -52,13 +52,20 @@ class Workload:
     p_zero: float      # probability of a zero weight
 
 
-# The five workloads: ragged forward, square forward, the pages' largest
-# forward shape, the 1782-row backward, and the small-M forward sweep.
+# The workloads: ragged forward, square forward, the pages' largest forward
+# shape, the 1782-row backward, the small-M forward sweep, and the other forward
+# shapes of the pages' throughput table ("t27c PTX backend: ternary x int8 GEMM
+# kernel emitted by a .t27 spec", section "Measured: RTX 4090"), M x N x K.
+PAGES_FWD_SHAPES = [(4096, 3456, 1280), (4096, 1280, 3456), (4096, 1280, 1280),
+                    (16384, 1280, 3456), (16384, 1280, 1280)]
 WORKLOADS = [
     Workload("fwd_ragged_300x272x96", "fwd", 300, 272, 96, 0, 1.0 / 3.0),
     Workload("fwd_square_4096", "fwd", 4096, 4096, 4096, 1, 0.5),
     Workload("fwd_16384x3456x1280", "fwd", 16384, 3456, 1280, 2, 1.0 / 3.0),
     Workload("bwd_1782x3456x1280", "bwd", 1782, 3456, 1280, 3, 1.0 / 3.0),
+] + [
+    Workload(f"fwd_{m}x{n}x{k}", "fwd", m, n, k, 5 + i, 1.0 / 3.0)
+    for i, (m, n, k) in enumerate(PAGES_FWD_SHAPES)
 ] + [
     Workload(f"skinny_m{m}_n{n}_k{k}", "skinny", m, n, k, 4, 1.0 / 3.0)
     for (n, k) in ((3456, 1280), (8192, 8192)) for m in (1, 8, 27)

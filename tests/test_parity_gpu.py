@@ -206,7 +206,8 @@ def test_adversarial_large_then_small_terms():
 # Every workload in the bench's launch configuration, every element compared
 # with the oracle.
 
-@pytest.mark.parametrize("name", ["fwd_square_4096", "fwd_16384x3456x1280"])
+@pytest.mark.parametrize("name", ["fwd_square_4096", "fwd_16384x3456x1280"] +
+                         [f"fwd_{m}x{n}x{k}" for (m, n, k) in t3_synth.PAGES_FWD_SHAPES])
 def test_full_size_forward(name):
     wl = t3_synth.BY_NAME[name]
     A, w, _ = workload_inputs(name)
