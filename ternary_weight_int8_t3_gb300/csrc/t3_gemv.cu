@@ -26,7 +26,8 @@
 //   * the lanes' int32 sums of a row are added with warp shuffles and one lane
 //     per (row, m) stores C[m][n].
 // Launch: a programmatic dependent of whatever precedes it on the stream; it
-// reads A and Wp and writes C only after griddepcontrol.wait.
+// reads A and Wp and writes C only after griddepcontrol.wait, and before the
+// wait asks its share of 16-byte aligned packed rows into L2.
 #include <atomic>
 #include <cstdint>
 
@@ -39,6 +40,8 @@ namespace gv {
 constexpr int kWarps = 16;                 // 512 threads, one CTA per SM
 constexpr uint32_t kWeightTable = 0x00FF0100u;  // code c -> byte c: 0, +1, -1, 0
 constexpr int64_t kMaxSmem = 64 * 1024;    // A's copy: M * ceil(K/64) * 64 bytes at most
+constexpr int64_t kPrefetchBytes = 48ll << 20;  // weights asked into L2 ahead, per call
+constexpr uint32_t kPrefetchPiece = 16384;
 
 // The four int8-weight words of 16 codes (code i at bits 2i of x), in the
 // order even codes 0..6 | 8..14, odd codes 1..7 | 9..15.
@@ -64,9 +67,25 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
   // j) read consecutive 16-byte entries
   extern __shared__ uint4 sa[];
   const int chunks4 = groups / 4;
-  launch_dependents();
-  grid_dependency_wait();  // A and Wp exist, and C is no longer read by the grid before
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // this CTA's rows: an equal contiguous share [nb, ne), taken R at a time by
+  // its warps in turn
+  const int64_t nb = static_cast<int64_t>(N) * blockIdx.x / gridDim.x;
+  const int64_t ne = static_cast<int64_t>(N) * (blockIdx.x + 1) / gridDim.x;
+  launch_dependents();
+  if (kVec) {
+    // the share's packed rows are contiguous: ask them into L2 while the grid
+    // before is still running (a hint only; the loads come after the wait)
+    int64_t bytes = (ne - nb) * KB;
+    const int64_t cap = kPrefetchBytes / gridDim.x / 16 * 16;
+    if (bytes > cap) bytes = cap;
+    const uint8_t* base = Wp + nb * KB;
+    for (int64_t off = static_cast<int64_t>(tid) * kPrefetchPiece; off < bytes;
+         off += static_cast<int64_t>(32 * kWarps) * kPrefetchPiece)
+      bulk_prefetch_l2(base + off, static_cast<uint32_t>(bytes - off < kPrefetchPiece ? bytes - off
+                                                                                      : kPrefetchPiece));
+  }
+  grid_dependency_wait();  // A and Wp exist, and C is no longer read by the grid before
   // rows of A in 16-byte pieces where they allow (K a multiple of 16, aligned)
   const bool a_vec = (K % 16 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
   for (int idx = tid; idx < MR * groups; idx += 32 * kWarps) {
@@ -93,10 +112,6 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
   }
   __syncthreads();
   const int64_t chunks = (KB + 15) / 16;
-  // this CTA's rows: an equal contiguous share [nb, ne), taken R at a time by
-  // its warps in turn
-  const int64_t nb = static_cast<int64_t>(N) * blockIdx.x / gridDim.x;
-  const int64_t ne = static_cast<int64_t>(N) * (blockIdx.x + 1) / gridDim.x;
   for (int64_t n0 = nb + static_cast<int64_t>(warp) * R; n0 < ne; n0 += kWarps * R) {
     int32_t acc[R][MR];
 #pragma unroll

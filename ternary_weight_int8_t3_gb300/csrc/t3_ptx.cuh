@@ -196,6 +196,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Asks for `bytes` (a multiple of 16) of global memory at a 16-byte aligned
+// address to be brought into L2.  A hint: nothing completes or is waited for,
+// and since L2 is where this GPU's writes meet, a later load still sees any
+// write that lands in between.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
 // Waits until the grids this one depends on programmatically have completed
 // and their writes are visible; a no-op without such a dependency.
 __device__ __forceinline__ void grid_dependency_wait() {
