@@ -149,15 +149,12 @@ __host__ __device__ constexpr uint32_t idesc_f16_mn(int m, int n) {
 }
 
 // One unit of one operand's stage: raw int8 row m (of 128), 16-byte chunk c
-// (16 MN values) -> two 8-value f16 chunks 2c, 2c+1 of MN-major atom c/4.
+// (16 MN values) -> two 8-value f16 chunks 2c, 2c+1 of MN-major atom c/4
+// (widen_store: the stores of the widened chunks lo, hi).
 // Threads c >= 4 write their odd chunk first so that each 8-thread store
 // phase hits 8 distinct bank groups.
-__device__ __forceinline__ void widen_unit(uint4 x, int m, int c, uint8_t* op) {
-  uint4 lo, hi;
-  tc::s8x4_to_f16(x.x, lo.x, lo.y);
-  tc::s8x4_to_f16(x.y, lo.z, lo.w);
-  tc::s8x4_to_f16(x.z, hi.x, hi.y);
-  tc::s8x4_to_f16(x.w, hi.z, hi.w);
+__device__ __forceinline__ void widen_store(const uint4 lo, const uint4 hi, int m, int c,
+                                            uint8_t* op) {
   const int r = m & 7;
   uint8_t* row = op + (m >> 3) * K_GROUP + (c >> 2) * MN_ATOM + r * 128;
   // selects, not a branch: a branch on c would split every warp and issue
@@ -170,16 +167,25 @@ __device__ __forceinline__ void widen_unit(uint4 x, int m, int c, uint8_t* op) {
   sts128(row + ((g ^ r) << 4), second);
 }
 
-// One operand of one stage: raw int8 [128 m][128 MN] -> f16 MN-major atoms.
-// Unit u = (row m, 16-byte raw chunk c), four per thread.
-__device__ __forceinline__ void widen_mn(const uint8_t* raw, uint8_t* op, int tid) {
-  constexpr int kUnits = BK * 8;
-#pragma unroll
-  for (int u = tid; u < kUnits; u += kHalfThreads) {
-    const int m = u >> 3, c = u & 7;
-    widen_unit(*reinterpret_cast<const uint4*>(raw + m * 128 + 16 * c), m, c, op);
-  }
+__device__ __forceinline__ void widen_regs(uint4 x, uint4& lo, uint4& hi) {
+  tc::s8x4_to_f16(x.x, lo.x, lo.y);
+  tc::s8x4_to_f16(x.y, lo.z, lo.w);
+  tc::s8x4_to_f16(x.z, hi.x, hi.y);
+  tc::s8x4_to_f16(x.w, hi.z, hi.w);
 }
+
+__device__ __forceinline__ void widen_unit(uint4 x, int m, int c, uint8_t* op) {
+  uint4 lo, hi;
+  widen_regs(x, lo, hi);
+  widen_store(lo, hi, m, c, op);
+}
+
+// Unit (row m, chunk c) of a raw stage [128 m][128 MN], widened in registers.
+__device__ __forceinline__ void widen_load(const uint8_t* raw, int m, int c, uint4& lo, uint4& hi) {
+  widen_regs(*reinterpret_cast<const uint4*>(raw + m * 128 + 16 * c), lo, hi);
+}
+
+// (row m, 16-byte chunk c) units of one operand's stage, four per converter thread
 constexpr int kUnitsPerThread = BK * 8 / kHalfThreads;
 static_assert(kUnitsPerThread == 4, "four units per converter thread");
 
@@ -282,18 +288,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
           continue;
         }
-        ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2) &&
-             mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
+        // widen as soon as the raw stage is in and release it; wait for the
+        // operand slot (freed when the MMAs two stages back complete) only
+        // before storing, so that the widening stays off the slot hand-off
+        ok = mbar_wait(&raw_full[rs], rph, abort_flag, p.err, code_base | 2);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         const uint8_t* r = raw + rs * RAW_STAGE + (a_warp ? 0 : RAW_OP);
+        uint4 lo[kUnitsPerThread], hi[kUnitsPerThread];
+#pragma unroll
+        for (int i = 0; i < kUnitsPerThread; ++i) {
+          const int u = htid + i * kHalfThreads;
+          widen_load(r, u >> 3, u & 7, lo[i], hi[i]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[rs]);
+        ok = mbar_wait(&op_empty[os], oph ^ 1u, abort_flag, p.err, code_base | 2);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         uint8_t* o = op + os * OP_STAGE + (a_warp ? 0 : OP_OPERAND);
-        widen_mn(r, o, htid);
+#pragma unroll
+        for (int i = 0; i < kUnitsPerThread; ++i) {
+          const int u = htid + i * kHalfThreads;
+          widen_store(lo[i], hi[i], u >> 3, u & 7, o);
+        }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&raw_empty[rs]);
-          mbar_arrive(&signal[os]);
-        }
+        if (lane == 0) mbar_arrive(&signal[os]);
         if (++rs == RAW_STAGES) { rs = 0; rph ^= 1u; }
         if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
       }
@@ -345,6 +364,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_f16_mn(BMP, BN);
       uint32_t os = 0, oph = 0, ab = 0, aph = 0;
       bool ok = true, issued_any = false;
+      const uint64_t adesc0 = smem_desc_mn_sw128(smem_addr(op), MN_ATOM, K_GROUP);
       for (int c = 0; ok && c < units.nc; ++c)
       for (int tile = units.t0; ok && tile <= units.t1; ++tile) {
         if (!units.has(tile, c)) continue;
@@ -355,19 +375,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + ab * BN;
-          for (int64_t kb = c0; kb < c1; ++kb) {
+          // 32-bit stage count and descriptors from slot 0's: the issuer's own
+          // work between its MMAs stays short
+          const int n_st = static_cast<int>(c1 - c0);
+          for (int st = 0; st < n_st; ++st) {
             ok = mbar_wait(&op_full[os], oph, abort_flag, p.err, code_base | 3);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t a0 = smem_addr(op + os * OP_STAGE);
-            const uint64_t adesc = smem_desc_mn_sw128(a0, MN_ATOM, K_GROUP);
-            const uint64_t bdesc = smem_desc_mn_sw128(a0 + OP_OPERAND, MN_ATOM, K_GROUP);
+            const uint64_t adesc = adesc0 + static_cast<uint64_t>((os * OP_STAGE) >> 4);
+            const uint64_t bdesc = adesc + static_cast<uint64_t>(OP_OPERAND >> 4);
             // K-step j covers m rows [16j, 16j + 16): two 8-row groups further on
 #pragma unroll
             for (int j = 0; j < BK / 16; ++j)
               umma_pair_ss(d_tmem, adesc + static_cast<uint64_t>((2 * j * K_GROUP) >> 4),
                            bdesc + static_cast<uint64_t>((2 * j * K_GROUP) >> 4), idesc,
-                           (kb > c0 || j > 0) ? 1u : 0u);
+                           (st > 0 || j > 0) ? 1u : 0u);
             issued_any = true;
             tc2::umma_commit_pair(&op_empty[os]);
             if (++os == OP_STAGES) { os = 0; oph ^= 1u; }
