@@ -77,38 +77,47 @@ __device__ __forceinline__ int32_t f32_bits_to_i32(uint32_t bits) {
   return __float2int_rn(__uint_as_float(bits));  // the value is an exact integer
 }
 
-// Writes (first chunk) or adds (later chunks) 32 values of one output row.
-__device__ __forceinline__ void store_row32(int32_t* dst, const uint32_t (&v)[32], int valid,
-                                            bool first, bool vec_ok) {
-  if (vec_ok && valid == 32) {
-#pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      int4 val = make_int4(f32_bits_to_i32(v[i]), f32_bits_to_i32(v[i + 1]),
-                           f32_bits_to_i32(v[i + 2]), f32_bits_to_i32(v[i + 3]));
-      int4* p = reinterpret_cast<int4*>(dst + i);
-      if (!first) {
-        const int4 old = *p;
-        val.x += old.x; val.y += old.y; val.z += old.z; val.w += old.w;
-      }
-      *p = val;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (i < valid) {
-        const int32_t val = f32_bits_to_i32(v[i]);
-        dst[i] = first ? val : dst[i] + val;
-      }
-    }
+// How out_block32 writes: store, add into elements only this warp writes
+// (read, add, write), or add atomically (other CTAs add into the same ones).
+enum OutBlockKind { kOutStore = 0, kOutAdd = 1, kOutAtomicAdd = 2 };
+
+// The row pass of out_block32, out of line: it runs only for outputs TMA
+// cannot address, and kept inline its loop adds to the register pressure of
+// every pipeline instantiation.
+static __device__ __noinline__ void out_rows32(const uint32_t* scratch, int lane, int32_t* out, int64_t ld,
+                                               int64_t row0, int64_t rows, int64_t col0, int64_t cols,
+                                               int kind) {
+  const bool col_ok = col0 + lane < cols;
+  const int64_t left = rows - row0;
+  const int nrows = left < 32 ? static_cast<int>(left) : 32;
+  int32_t* dst = out + row0 * ld + col0 + lane;
+  for (int r = 0; r < nrows; ++r, dst += ld) {
+    const int32_t x = f32_bits_to_i32(scratch[r * 33 + lane]);
+    if (!col_ok) continue;
+    if (kind == kOutStore)
+      *dst = x;
+    else if (kind == kOutAdd)
+      *dst += x;
+    else
+      atomicAdd(dst, x);
   }
 }
 
-// Adds a row of up to 32 exact sums (f32 bit patterns) into int32 output
-// elements that other CTAs also add into.
-__device__ __forceinline__ void atomic_add_row32(int32_t* dst, const uint32_t (&v)[32], int valid) {
+// A warp's 32 x 32 block of exact sums (f32 bit patterns) into int32 rows of
+// any alignment: lane l holds row row0 + l, columns col0 .. col0 + 31, in v.
+// The block is transposed through `scratch` (33 x 32 words of this warp's
+// own shared memory; the odd pitch keeps both passes free of bank conflicts)
+// so that each instruction writes 32 consecutive columns of one row, one or
+// two memory transactions, instead of touching 32 rows.  Rows from `rows`
+// on and columns from `cols` on are left alone.
+__device__ __forceinline__ void out_block32(uint32_t* scratch, const uint32_t (&v)[32], int lane,
+                                            int32_t* out, int64_t ld, int64_t row0, int64_t rows,
+                                            int64_t col0, int64_t cols, int kind) {
+  __syncwarp();  // the previous block's reads of scratch are done
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (i < valid) atomicAdd(dst + i, f32_bits_to_i32(v[i]));
+  for (int j = 0; j < 32; ++j) scratch[lane * 33 + j] = v[j];
+  __syncwarp();
+  out_rows32(scratch, lane, out, ld, row0, rows, col0, cols, kind);
 }
 
 }  // namespace tc

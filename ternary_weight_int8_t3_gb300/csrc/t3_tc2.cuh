@@ -86,6 +86,8 @@ template <int OP, int kActBytes = 1> struct Layout {
   static constexpr int off_misc = off_bar + 8 * n_bars;
   static constexpr int smem_alloc = off_misc + 16 + 1024;
 };
+static_assert(4 * 33 * 32 * 4 <= 2 * Layout<kOpFwd>::stage_out,
+              "the unaligned-output epilogue's row blocks fit the staging buffers");
 
 // Output kind of the pair pipeline: the exact int32 product, or (one exact
 // chunk only, bulk stores only) the scaled forms of t3_dequant_i32.
@@ -978,7 +980,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int epi_tid = threadIdx.x - kEpiWarp0 * 32;
     const int srow = q * 32 + lane;
     const uint32_t acc_empty_leader0 = peer_addr(&acc_empty[0], 0);
-    const bool vec_ok = (p.out_cols % 4 == 0) && (reinterpret_cast<uintptr_t>(p.out) % 16 == 0);
     uint32_t ab = 0, aph = 0, slab = 0;
     bool ok = true;
     if (p.use_tma_out && epi_tid == 0) prefetch_tensormap(&map_out);
@@ -1055,13 +1056,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               bulk_commit_group();
             }
             ++slab;
-          } else if (row < p.out_rows) {
-            const int64_t rem = p.out_cols - col0;
-            const int valid = rem < 32 ? static_cast<int>(rem) : 32;
-            if (sk)  // other pairs add into the same elements
-              tc::atomic_add_row32(p.out + row * p.out_cols + col0, v, valid);
-            else
-              tc::store_row32(p.out + row * p.out_cols + col0, v, valid, first, vec_ok);
+          } else {
+            // rows TMA cannot address (int32 only): row by row through this
+            // warp's part of the idle staging buffers; stream-K pieces add
+            // atomically (other pairs add into the same elements)
+            uint32_t* scratch = reinterpret_cast<uint32_t*>(stage_out) + q * (33 * 32);
+            tc::out_block32(scratch, v, lane, p.out, p.out_cols, row0 + q * 32, p.out_rows, col0,
+                            p.out_cols, sk ? tc::kOutAtomicAdd : (first ? tc::kOutStore : tc::kOutAdd));
           }
         }
         tc_fence_before();

@@ -72,6 +72,7 @@ constexpr int N_BARS = 2 * RAW_STAGES + 3 * OP_STAGES + 2 * ACC_BUFS + 1;
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
 constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+static_assert(4 * 33 * 32 * 4 <= 2 * STAGE_OUT, "unaligned-output row blocks fit the staging buffers");
 
 struct Params {
   int64_t M, N, K;       // the product's sizes: reduction M, dW [K][N]
@@ -458,13 +459,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              v);
           tmem_wait_ld();
           if (!p.use_tma_out) {
-            // rows of dW not 16-byte aligned: one atomic add per element
-            const int64_t row = static_cast<int64_t>(row0) + srow;
-            if (row < p.K) {
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (col0 + e < p.N) atomicAdd(p.out + row * p.N + col0 + e, tc::f32_bits_to_i32(v[e]));
-            }
+            // rows of dW not 16-byte aligned: atomic adds row by row, through
+            // this warp's part of the idle staging buffers
+            uint32_t* scratch = reinterpret_cast<uint32_t*>(stage_out) + q * (33 * 32);
+            tc::out_block32(scratch, v, lane, p.out, p.N, row0 + q * 32, p.K, col0, p.N,
+                            tc::kOutAtomicAdd);
             continue;
           }
           uint8_t* buf = stage_out + (slab & 1) * STAGE_OUT;
