@@ -108,6 +108,13 @@ int t3_pack_ternary_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N,
  * TMA-addressable, the reduction of the last tiles is split over the whole
  * GPU: the call then enqueues the same pair of kernels, the first zeroing the
  * rows of C that the split part adds into.
+ * Small products (M*N*K at most the limit of t3_set_small_product_limit,
+ * 2^29 by default, when a row stride or base of A or Wp is not a multiple of
+ * 16 bytes, else at most an eighth of it; for M <= 32 only the first case)
+ * run on the CUDA cores instead: 64 x 64 output tiles, the reduction split
+ * over CTAs that add atomically onto a zeroed C when the tiles are few (a
+ * cudaMemsetAsync and one kernel, both on `stream`, in stream order), any
+ * alignment of A, Wp and C.
  */
 int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,
                 int64_t K, t3_stream_t stream);
@@ -117,7 +124,8 @@ int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64
  *   dY [M][N], Wp [N][ceil(K/4)] (the forward's packed weights), dX [M][K].
  * Exact for every input when N <= 16777215; larger N returns T3_EOVERFLOW.
  * Long reductions over few output tiles are split as in t3_gemm_fwd (M > 32),
- * with a zeroing kernel before the product.
+ * with a zeroing kernel before the product.  Small products run on the CUDA
+ * cores as in t3_gemm_fwd.
  */
 int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, int64_t N,
                    int64_t K, t3_stream_t stream);
@@ -130,7 +138,8 @@ int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, 
  * It enqueues two kernels on `stream`: one that zeroes dW and one that adds
  * 1024-row partial sums into it; the second may start before the first ends
  * (programmatic dependent launch) but touches dW only after it, and the first
- * touches dW only after all earlier work on `stream`.
+ * touches dW only after all earlier work on `stream`.  Small products run on
+ * the CUDA cores as in t3_gemm_fwd.
  */
 int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, int64_t N,
                    int64_t K, t3_stream_t stream);
@@ -272,6 +281,20 @@ const char* t3_status_string(int status);
  * packer; 10 the wait self-test below).
  */
 int t3_last_device_error(t3_stream_t stream, int32_t* detail);
+
+/*
+ * t3_set_small_product_limit -- the route of t3_gemm_fwd, t3_gemm_bwd_dx and
+ * t3_gemm_bwd_dw (and of their scaled forms' int32 pass): products of at most
+ * `macs` multiply-adds (M*N*K) run on the CUDA cores when an operand's rows
+ * are not TMA-addressable (stride or base not a multiple of 16 bytes), of at
+ * most macs / 8 when they all are; larger ones on the tensor cores.  Default
+ * 2^29 (536870912); 0 sends every product to the tensor cores; negative
+ * values count as 0.  Process-wide, for every device;
+ * a call racing with products on other threads may see either route, and
+ * both give the same exact result.  Returns the previous limit.  Host only:
+ * no CUDA call, no error.
+ */
+int64_t t3_set_small_product_limit(int64_t macs);
 
 /*
  * t3_selftest_wait_timeout -- exercises the bounded-wait path above without

@@ -86,6 +86,8 @@ def load():
         lib.t3_last_device_error.restype = ctypes.c_int
         lib.t3_selftest_wait_timeout.argtypes = [i64, p]
         lib.t3_selftest_wait_timeout.restype = ctypes.c_int
+        lib.t3_set_small_product_limit.argtypes = [i64]
+        lib.t3_set_small_product_limit.restype = i64
         lib.t3_version.argtypes = []
         lib.t3_version.restype = ctypes.c_int
         _lib = lib
@@ -408,6 +410,14 @@ def t3_last_device_error(stream=None):
     detail = ctypes.c_int32(0)
     rc = load().t3_last_device_error(ctypes.c_void_p(s.cuda_stream), ctypes.byref(detail))
     return rc, detail.value
+
+
+def t3_set_small_product_limit(macs: int) -> int:
+    """Products of at most `macs` multiply-adds (macs / 8 when every operand's
+    rows are TMA-addressable) run on the CUDA cores, larger ones on the tensor
+    cores (default 2**29; 0: always the tensor cores).  Returns the previous
+    limit."""
+    return int(load().t3_set_small_product_limit(int(macs)))
 
 
 def t3_selftest_wait_timeout(limit_ns: int, stream=None):

@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libt3.so")
 
 SOURCES = ["t3_api.cu", "t3_tc_fwd.cu", "t3_tc_dx.cu", "t3_tc_dw.cu", "t3_skinny.cu", "t3_pack.cu", "t3_dequant.cu", "t3_quant.cu",
-           "t3_noalloc.cu", "t3_gemv.cu"]
+           "t3_noalloc.cu", "t3_gemv.cu", "t3_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-Xptxas", "-v",
          "-I", os.path.join(ROOT, "include")]

@@ -335,6 +335,34 @@ int scaled_two_pass(Product product, void* out, int64_t rows, int64_t cols, cons
   return launch_dequant(x, out, rows, cols, row_scale, col_scale, kind, dev->sms, stream);
 }
 
+// Products of at most this many multiply-adds run on the CUDA cores
+// (t3_small.cu) when an operand's rows are not TMA-addressable, and of at most
+// an eighth of it when all are: the CTA-pair pipelines then load such rows
+// byte by byte (the pages' HSLM layers, widths 243 and 729 at 1782 rows:
+// 15-26 us on the CUDA cores against 21-74 us), while with TMA operands they
+// stay ahead down to a few 10^7 (the same layers padded to 256 and 736: 8-15
+// against 13-18 us).  Set with t3_set_small_product_limit.
+std::atomic<int64_t> g_small_macs{int64_t{1} << 29};
+
+bool small_product(int64_t a, int64_t b, int64_t c, bool tma_rows) {
+  int64_t lim = g_small_macs.load(std::memory_order_relaxed);
+  if (tma_rows) lim /= 8;
+  return static_cast<__int128>(a) * b * c <= static_cast<__int128>(lim);
+}
+
+// Rows of `len` bytes from `base` that a TMA map can address.
+bool tma_rows(const void* base, int64_t len) {
+  return len % 16 == 0 && reinterpret_cast<uintptr_t>(base) % 16 == 0;
+}
+
+int run_small(int op, const int8_t* x, const int8_t* y, const uint8_t* wp, int32_t* out, int64_t M,
+              int64_t N, int64_t K, cudaStream_t stream) {
+  const DeviceInfo* dev = nullptr;
+  const int st = device_info(&dev);
+  if (st != T3_OK) return st;
+  return launch_small(op, x, y, wp, out, M, N, K, dev->sms, stream);
+}
+
 bool bad_dims(int64_t M, int64_t N, int64_t K) {
   return M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim;
 }
@@ -397,8 +425,15 @@ int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64
       st = launch_gemv_fwd(A, Wp, C, M, N, K, dev->sms, stream);
       if (st != T3_EINVAL) return st;
     }
+    // packed rows the small-M kernel's TMA cannot address: it would load them
+    // byte by byte in one warp
+    const bool wp_tma = tma_rows(Wp, (K + 3) / 4);
+    if (!wp_tma && small_product(M, N, K, false))
+      return run_small(1, A, nullptr, Wp, C, M, N, K, stream);
     return launch_skinny_fwd(A, Wp, C, M, N, K, dev->sms, dev->err_word, stream);
   }
+  if (small_product(M, N, K, tma_rows(A, K) && tma_rows(Wp, (K + 3) / 4)))
+    return run_small(1, A, nullptr, Wp, C, M, N, K, stream);
   return run_tc2<kOpFwd>(A, Wp, C, M, N, K, stream);
 }
 
@@ -409,6 +444,8 @@ int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, 
   if (N == 0) return zero_fill(dX, M, K, stream);
   if (!dY || !Wp || !dX) return T3_EINVAL;
   if (N > kMaxTernaryReduction) return T3_EOVERFLOW;
+  if (small_product(M, N, K, tma_rows(dY, N) && tma_rows(Wp, (K + 3) / 4)))
+    return run_small(2, dY, nullptr, Wp, dX, M, N, K, stream);
   return run_tc2<kOpDx>(dY, Wp, dX, M, N, K, stream);
 }
 
@@ -419,6 +456,8 @@ int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, in
   if (M == 0) return zero_fill(dW, K, N, stream);
   if (!A || !dY || !dW) return T3_EINVAL;
   if (M > kMaxInt8Reduction) return T3_EOVERFLOW;
+  if (small_product(M, N, K, tma_rows(A, K) && tma_rows(dY, N)))
+    return run_small(3, A, dY, nullptr, dW, M, N, K, stream);
   return run_dw2(A, dY, dW, M, N, K, stream);
 }
 
@@ -502,6 +541,10 @@ int t3_gemm_bwd_dw_scaled(const int8_t* A, const int8_t* dY, void* dW, int64_t M
   return scaled_two_pass(
       [&](int32_t* x) { return t3_gemm_bwd_dw(A, dY, x, M, N, K, stream); }, dW, K, N, row_scale,
       col_scale, out_kind, workspace, stream);
+}
+
+int64_t t3_set_small_product_limit(int64_t macs) {
+  return g_small_macs.exchange(macs < 0 ? 0 : macs);
 }
 
 }  // extern "C"

@@ -67,6 +67,13 @@ int launch_dequant(const int32_t* x, void* out, int64_t rows, int64_t cols, cons
 int launch_gemv_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,
                     int64_t K, int sms, cudaStream_t s);
 
+// The three products on the CUDA cores for small problems, any alignment
+// (t3_small.cu): op 1 C = A.W (x = A, wp = Wp), 2 dX = dY.Wᵀ (x = dY, wp = Wp),
+// 3 dW = Aᵀ.dY (x = A, y = dY); int32 output, written whole (zeroed first
+// when the reduction is split over CTAs).
+int launch_small(int op, const int8_t* x, const int8_t* y, const uint8_t* wp, int32_t* out,
+                 int64_t M, int64_t N, int64_t K, int sms, cudaStream_t s);
+
 // Small-M forward (M <= 32) on the tensor cores.
 int launch_skinny_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64_t N,
                       int64_t K, int sms, int* err, cudaStream_t s);

@@ -46,6 +46,16 @@ def test_selftest_rejects_limits_out_of_range_before_any_cuda_call(lib):
         assert f(limit, None) == t3.T3_EINVAL
 
 
+def test_small_product_limit_round_trips_without_a_gpu(lib):
+    prev = t3.t3_set_small_product_limit(12345)
+    try:
+        assert prev >= 0
+        assert t3.t3_set_small_product_limit(-7) == 12345
+        assert t3.t3_set_small_product_limit(1 << 29) == 0  # negative counts as 0
+    finally:
+        t3.t3_set_small_product_limit(prev)
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, -6):
         s = t3.status_string(code)
