@@ -110,7 +110,8 @@ int t3_pack_ternary_device(const int8_t* w, uint8_t* wp, int64_t K, int64_t N,
  * rows of C that the split part adds into.
  * Small products (M*N*K at most the limit of t3_set_small_product_limit,
  * 2^29 by default, when a row stride or base of A or Wp is not a multiple of
- * 16 bytes, else at most an eighth of it; for M <= 32 only the first case)
+ * 4 bytes, else at most an eighth of it; for M <= 32 only when Wp's rows are
+ * not 16-byte multiples on a 16-byte boundary)
  * run on the CUDA cores instead: 64 x 64 output tiles, the reduction split
  * over CTAs that add atomically onto a zeroed C when the tiles are few (a
  * cudaMemsetAsync and one kernel, both on `stream`, in stream order), any
@@ -286,7 +287,7 @@ int t3_last_device_error(t3_stream_t stream, int32_t* detail);
  * t3_set_small_product_limit -- the route of t3_gemm_fwd, t3_gemm_bwd_dx and
  * t3_gemm_bwd_dw (and of their scaled forms' int32 pass): products of at most
  * `macs` multiply-adds (M*N*K) run on the CUDA cores when an operand's rows
- * are not TMA-addressable (stride or base not a multiple of 16 bytes), of at
+ * are not 4-byte aligned (stride or base not a multiple of 4 bytes), of at
  * most macs / 8 when they all are; larger ones on the tensor cores.  Default
  * 2^29 (536870912); 0 sends every product to the tensor cores; negative
  * values count as 0.  Process-wide, for every device;

@@ -414,7 +414,7 @@ def t3_last_device_error(stream=None):
 
 def t3_set_small_product_limit(macs: int) -> int:
     """Products of at most `macs` multiply-adds (macs / 8 when every operand's
-    rows are TMA-addressable) run on the CUDA cores, larger ones on the tensor
+    rows are 4-byte aligned) run on the CUDA cores, larger ones on the tensor
     cores (default 2**29; 0: always the tensor cores).  Returns the previous
     limit."""
     return int(load().t3_set_small_product_limit(int(macs)))

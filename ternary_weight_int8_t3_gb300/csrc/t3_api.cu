@@ -336,23 +336,24 @@ int scaled_two_pass(Product product, void* out, int64_t rows, int64_t cols, cons
 }
 
 // Products of at most this many multiply-adds run on the CUDA cores
-// (t3_small.cu) when an operand's rows are not TMA-addressable, and of at most
-// an eighth of it when all are: the CTA-pair pipelines then load such rows
-// byte by byte (the pages' HSLM layers, widths 243 and 729 at 1782 rows:
-// 15-26 us on the CUDA cores against 21-74 us), while with TMA operands they
-// stay ahead down to a few 10^7 (the same layers padded to 256 and 736: 8-15
-// against 13-18 us).  Set with t3_set_small_product_limit.
+// (t3_small.cu) when an operand's rows are not 4-byte aligned, and of at most
+// an eighth of it otherwise: the CTA-pair pipelines load rows that are not
+// even word-aligned byte by byte (the pages' HSLM layers, widths 243 and 729
+// at 1782 rows: 15-26 us on the CUDA cores against 21-74 us), while with TMA
+// or word loads they stay ahead down to a few 10^7 (the same layers padded to
+// 256 and 736: 8.5-14.6 against 13-18 us).  Set with
+// t3_set_small_product_limit.
 std::atomic<int64_t> g_small_macs{int64_t{1} << 29};
 
-bool small_product(int64_t a, int64_t b, int64_t c, bool tma_rows) {
+bool small_product(int64_t a, int64_t b, int64_t c, bool aligned) {
   int64_t lim = g_small_macs.load(std::memory_order_relaxed);
-  if (tma_rows) lim /= 8;
+  if (aligned) lim /= 8;
   return static_cast<__int128>(a) * b * c <= static_cast<__int128>(lim);
 }
 
-// Rows of `len` bytes from `base` that a TMA map can address.
-bool tma_rows(const void* base, int64_t len) {
-  return len % 16 == 0 && reinterpret_cast<uintptr_t>(base) % 16 == 0;
+// Rows of `len` bytes from `base`, every one starting on a 4-byte boundary.
+bool word_rows(const void* base, int64_t len) {
+  return len % 4 == 0 && reinterpret_cast<uintptr_t>(base) % 4 == 0;
 }
 
 int run_small(int op, const int8_t* x, const int8_t* y, const uint8_t* wp, int32_t* out, int64_t M,
@@ -427,12 +428,13 @@ int t3_gemm_fwd(const int8_t* A, const uint8_t* Wp, int32_t* C, int64_t M, int64
     }
     // packed rows the small-M kernel's TMA cannot address: it would load them
     // byte by byte in one warp
-    const bool wp_tma = tma_rows(Wp, (K + 3) / 4);
+    const bool wp_tma =
+        ((K + 3) / 4) % 16 == 0 && reinterpret_cast<uintptr_t>(Wp) % 16 == 0;
     if (!wp_tma && small_product(M, N, K, false))
       return run_small(1, A, nullptr, Wp, C, M, N, K, stream);
     return launch_skinny_fwd(A, Wp, C, M, N, K, dev->sms, dev->err_word, stream);
   }
-  if (small_product(M, N, K, tma_rows(A, K) && tma_rows(Wp, (K + 3) / 4)))
+  if (small_product(M, N, K, word_rows(A, K) && word_rows(Wp, (K + 3) / 4)))
     return run_small(1, A, nullptr, Wp, C, M, N, K, stream);
   return run_tc2<kOpFwd>(A, Wp, C, M, N, K, stream);
 }
@@ -444,7 +446,7 @@ int t3_gemm_bwd_dx(const int8_t* dY, const uint8_t* Wp, int32_t* dX, int64_t M, 
   if (N == 0) return zero_fill(dX, M, K, stream);
   if (!dY || !Wp || !dX) return T3_EINVAL;
   if (N > kMaxTernaryReduction) return T3_EOVERFLOW;
-  if (small_product(M, N, K, tma_rows(dY, N) && tma_rows(Wp, (K + 3) / 4)))
+  if (small_product(M, N, K, word_rows(dY, N) && word_rows(Wp, (K + 3) / 4)))
     return run_small(2, dY, nullptr, Wp, dX, M, N, K, stream);
   return run_tc2<kOpDx>(dY, Wp, dX, M, N, K, stream);
 }
@@ -456,7 +458,7 @@ int t3_gemm_bwd_dw(const int8_t* A, const int8_t* dY, int32_t* dW, int64_t M, in
   if (M == 0) return zero_fill(dW, K, N, stream);
   if (!A || !dY || !dW) return T3_EINVAL;
   if (M > kMaxInt8Reduction) return T3_EOVERFLOW;
-  if (small_product(M, N, K, tma_rows(A, K) && tma_rows(dY, N)))
+  if (small_product(M, N, K, word_rows(A, K) && word_rows(dY, N)))
     return run_small(3, A, dY, nullptr, dW, M, N, K, stream);
   return run_dw2(A, dY, dW, M, N, K, stream);
 }

@@ -92,7 +92,7 @@ def test_split_reduction_adds_onto_zeros(op):
     over many CTAs that add atomically; the output starts as garbage."""
     g = t3_synth.rng(21)
     if op == "fwd":
-        M, N, K = 40, 70, 60000
+        M, N, K = 40, 70, 60001  # rows of A not word-aligned: the CUDA cores up to 2^29
         A = t3_synth.int8_uniform(g, (M, K))
         wp = t3_synth.raw_bytes(g, (N, (K + 3) // 4))
         C = torch.full((M, N), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
@@ -143,7 +143,7 @@ def test_int32_bounds():
 def test_both_sides_of_the_limit_agree():
     """The same small products through the CUDA cores (default limit) and
     through the tensor cores (limit 0): identical int32 outputs."""
-    M, N, K = 700, 300, 520
+    M, N, K = 700, 301, 519  # rows of A, dY and Wp not word-aligned: all three on the CUDA cores
     g = t3_synth.rng(31)
     A = _dev(t3_synth.int8_uniform(g, (M, K)))
     dY = _dev(t3_synth.int8_uniform(g, (M, N)))
