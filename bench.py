@@ -482,6 +482,62 @@ def bench_configs(t3, torch, dev, stream, peak, reps=20,
     return out
 
 
+# The layer widths of the pages' HSLM backward measurements (243 and 729, at
+# 27 and 1782 rows): rows of 243 and 729 bytes, not word-aligned.
+HSLM_SHAPES = [(m, n, k) for m in (27, 1782) for (n, k) in ((729, 243), (243, 729))]
+
+
+def bench_hslm(t3, torch, dev, peak, reps=20, max_sets=64):
+    """fwd, dX and dW at the HSLM widths, each product's calls captured in a
+    CUDA graph and replayed (these products take microseconds: without the
+    graph the host's launch rate would be timed).  Up to `max_sets` buffer
+    sets rotate through the calls; `set_bytes` x `buffer_sets` says whether
+    that rotation outgrows the 129 MB L2 (the 27-row shapes stay resident)."""
+    out = {}
+    for (m, n, k) in HSLM_SHAPES:
+        g = t3_synth.rng(m + n + k)
+        A = t3_synth.int8_uniform(g, (m, k))
+        dY = t3_synth.int8_uniform(g, (m, n))
+        wp = t3.t3_pack_ternary(t3_synth.ternary(g, (k, n)))
+        set_bytes = A.nbytes + dY.nbytes + wp.nbytes + 4 * (m * n + m * k + k * n)
+        sets = int(min(max_sets, max(2, -(-2 * 129 * 2**20 // set_bytes))))
+        bufs = [(torch.from_numpy(A).to(dev), torch.from_numpy(dY).to(dev), torch.from_numpy(wp).to(dev),
+                 torch.empty((m, n), dtype=torch.int32, device=dev),
+                 torch.empty((m, k), dtype=torch.int32, device=dev),
+                 torch.empty((k, n), dtype=torch.int32, device=dev)) for _ in range(sets)]
+        row = {"buffer_sets": sets, "set_bytes": set_bytes}
+        for prod in ("fwd", "dx", "dw"):
+            def call(b):
+                a_d, dy_d, wp_d, c_d, dx_d, dw_d = b
+                if prod == "fwd":
+                    t3.t3_gemm_fwd(a_d, wp_d, K=k, C=c_d)
+                elif prod == "dx":
+                    t3.t3_gemm_bwd_dx(dy_d, wp_d, k, dX=dx_d)
+                else:
+                    t3.t3_gemm_bwd_dw(a_d, dy_d, dW=dw_d)
+            for i in range(3):
+                call(bufs[i % sets])
+            torch.cuda.synchronize(dev)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                for i in range(reps):
+                    call(bufs[i % sets])
+            gr.replay()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            gr.replay()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            tops = 2 * m * n * k / (us * 1e-6) / 1e12
+            row[prod] = {"us": round(us, 2), "TOPS": round(tops, 2), "frac": round(tops / peak, 4)}
+            del gr
+        out[f"{m}x{n}x{k}"] = row
+        del bufs
+    return out
+
+
 def cpu_baseline(A, w, dY, target_s=15.0):
     """The oracle, as it stands, on a bounded sample of rows of each product."""
     import oracle
@@ -776,6 +832,7 @@ def main():
             shape = tuple(int(x) for x in key.split()[1].split("x"))
             v["pages_rtx4090_us"] = round(PAGES_FWD_MS[shape] * 1e3, 1)
         line["pages_fwd_shapes"] = pages
+        line["hslm_shapes"] = bench_hslm(t3, torch, dev, peak)
     if not (args.no_pack or args.step_only):
         line["device_pack"] = {"hbm_peak_GBps": hbm, "calls": bench_device_pack(t3, torch, dev, stream, hbm)}
     if not (args.no_small_m or args.step_only):
