@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--small-m-only", metavar="M,N,K", default=None,
                     help="time one small-M forward configuration of the sweep and exit "
                          "(for profiler captures)")
+    ap.add_argument("--hslm-only", metavar="M,N,K", default=None,
+                    help="time the three products at one of the HSLM shapes and exit "
+                         "(for profiler captures)")
     return ap.parse_args()
 
 
@@ -487,14 +490,14 @@ def bench_configs(t3, torch, dev, stream, peak, reps=20,
 HSLM_SHAPES = [(m, n, k) for m in (27, 1782) for (n, k) in ((729, 243), (243, 729))]
 
 
-def bench_hslm(t3, torch, dev, peak, reps=20, max_sets=64):
+def bench_hslm(t3, torch, dev, peak, reps=20, max_sets=64, shapes=None):
     """fwd, dX and dW at the HSLM widths, each product's calls captured in a
     CUDA graph and replayed (these products take microseconds: without the
     graph the host's launch rate would be timed).  Up to `max_sets` buffer
     sets rotate through the calls; `set_bytes` x `buffer_sets` says whether
     that rotation outgrows the 129 MB L2 (the 27-row shapes stay resident)."""
     out = {}
-    for (m, n, k) in HSLM_SHAPES:
+    for (m, n, k) in (shapes or HSLM_SHAPES):
         g = t3_synth.rng(m + n + k)
         A = t3_synth.int8_uniform(g, (m, k))
         dY = t3_synth.int8_uniform(g, (m, n))
@@ -624,6 +627,14 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
+
+    if args.hslm_only:
+        cfg = tuple(int(x) for x in args.hslm_only.split(","))
+        if cfg not in HSLM_SHAPES:
+            raise SystemExit(f"--hslm-only: {cfg} is not one of {HSLM_SHAPES}")
+        peak = read_peaks()[0].get("bf16_tflops", 1900.0)
+        print(json.dumps({"hslm_shapes": bench_hslm(t3, torch, dev, peak, shapes=[cfg])}))
+        return
 
     if args.small_m_only:
         cfg = tuple(int(x) for x in args.small_m_only.split(","))
